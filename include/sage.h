@@ -1,0 +1,209 @@
+/*
+ * sage.h - C ABI of a GB300 (sm_103a) implementation of SageAttention-style
+ * quantized, non-causal attention on BF16 [B, S, H, 128] inputs.
+ *
+ * The operation (sources are web pages, cited by title and section):
+ *
+ *  - "aiter-sage-attention: SageAttention for AMD RDNA4 (gfx1201) #1222",
+ *    section "The kernel": QK^T is computed in INT8 and PV in FP8, both with
+ *    FP32 accumulation; Q and K are quantized per 32-row block and V per
+ *    channel. Section "What I have so far": the entry
+ *    sageattn(q, k, v, tensor_layout, is_causal, sm_scale, return_lse) raises
+ *    on causal, LSE, non-BF16, head dim other than 128 and unequal Q/K/V
+ *    shapes instead of falling back silently.
+ *  - "Hand-written prologue: faster short calls, no compiler, RX 9060 XT
+ *    opt-in (v0.4.0)", section "What changed": the quantization prologue
+ *    uses 64-bit offsets (no sequence-length ceiling) and, with smooth_k on,
+ *    sums the key mean in fp64.
+ *  - "gfx1201 (RDNA4) SageAttention attention backend: aiter package or Hub
+ *    kernel?", section "原因分析" (cause analysis): BF16 [B, S, H, 128],
+ *    Q/K/V of one shape, no mask, not causal.
+ *
+ * Arithmetic fixed by this library where the pages are silent (the same
+ * readings the test oracle follows):
+ *  - Q and K: one fp32 scale per 32 consecutive tokens of one (batch, head)
+ *    over all 128 channels, s = amax / 127; code = rint_even(x / s) with x / s
+ *    correctly rounded in fp32, in [-127, 127]. K is first reduced by its
+ *    per-channel mean when smooth_k is on: k' = fl32(k - mean).
+ *  - Key mean: per 32-token chunk a left-to-right fp64 sum from +0.0, chunk
+ *    sums combined by a pairwise tree; mean = fl32(total / S) in fp64.
+ *  - V: one fp32 scale per (batch, head, channel) over all tokens,
+ *    s_v = amax / 448; code = e4m3fn(v / s_v), round to nearest even,
+ *    saturating to +-448.
+ *  - Attention: logits = S_int * (s_q * s_k) * sm_scale, online softmax in
+ *    fp32 over 128-key tiles in ascending order with the exact running
+ *    maximum; P stored as e4m3(448 * p); the row sum uses the unquantized p;
+ *    O = acc / l * s_v / 448, rounded to bf16 in the input layout.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev are CUDA device pointers; the caller owns every
+ *    buffer. The library allocates no memory and keeps no state between
+ *    calls except one device-side error word per GPU (see sage_device_error).
+ *  - Work is enqueued on the caller's stream (a cudaStream_t passed as
+ *    void*; NULL is the legacy default stream) and runs asynchronously; the
+ *    call returns once the work is enqueued.
+ *  - Sizes are int64_t. Every offset inside the kernels is 64-bit.
+ *  - Return value: SAGE_OK (0) or a negative SAGE_ERR_* code. Arguments are
+ *    validated before anything is enqueued; on error nothing is launched.
+ *    There is no fallback path of any kind.
+ *  - S_pad = ceil(S / 128) * 128 (one key tile). Padded code rows/columns
+ *    and padded scale blocks are written as zero.
+ *  - S = 0 (or B = 0 or H = 0) is an empty problem: validated, nothing
+ *    launched, SAGE_OK.
+ */
+#ifndef SAGE_H
+#define SAGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* Symbols of the shared library are hidden except these entry points. */
+#if defined(__GNUC__)
+#define SAGE_API __attribute__((visibility("default")))
+#else
+#define SAGE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- errors -- */
+enum {
+  SAGE_OK = 0,
+  SAGE_ERR_CAUSAL = -1,         /* is_causal != 0 (no mask support) */
+  SAGE_ERR_LSE = -2,            /* return_lse != 0 */
+  SAGE_ERR_DTYPE = -3,          /* an input or output is not BF16 */
+  SAGE_ERR_HEAD_DIM = -4,       /* D != 128 */
+  SAGE_ERR_SHAPE = -5,          /* Q, K, V shapes differ, or a size is negative */
+  SAGE_ERR_LAYOUT = -6,         /* tensor_layout is neither "NHD" nor "HND", or channel stride != 1 */
+  SAGE_ERR_ALIGN = -7,          /* a base pointer is not 16-byte aligned, or a stride is not a multiple of 8 elements */
+  SAGE_ERR_NULLPTR = -8,        /* a required pointer is NULL */
+  SAGE_ERR_WORKSPACE = -9,      /* workspace or scratch smaller than required */
+  SAGE_ERR_ARCH = -10,          /* current device is not compute capability 10.3 */
+  SAGE_ERR_CUDA = -11,          /* a CUDA runtime call or kernel launch failed */
+  SAGE_ERR_DEVICE_TIMEOUT = -12,/* a kernel gave up waiting on an internal barrier (see sage_device_error) */
+  SAGE_ERR_ARG = -13,           /* another invalid argument (e.g. non-finite or non-positive sm_scale) */
+  SAGE_ERR_TOO_LARGE = -14      /* sizes exceed the library's index limits */
+};
+
+/* dtype codes for sage_sageattn */
+enum { SAGE_DTYPE_BF16 = 0, SAGE_DTYPE_F16 = 1, SAGE_DTYPE_F32 = 2, SAGE_DTYPE_OTHER = 3 };
+
+/* ------------------------------------------------------------ data types -- */
+
+/* One BF16 input tensor: element (b, s, h, d) lives at
+ *   ptr_dev + b*stride_b + s*stride_s + h*stride_h + d      (in elements).
+ * The channel stride is 1. "NHD" ([B,S,H,D], contiguous) has
+ * stride_b = S*H*D, stride_s = H*D, stride_h = D; "HND" ([B,H,S,D]) has
+ * stride_b = H*S*D, stride_h = S*D, stride_s = D. */
+typedef struct sage_bf16_tensor {
+  const void* ptr_dev;
+  int64_t stride_b, stride_s, stride_h;
+} sage_bf16_tensor;
+
+/* The quantized bundle written by sage_quantize and read by sage_attention.
+ * All pointers are device pointers, 16-byte aligned.
+ *   q_codes, k_codes : int8   [B][H][S_pad][128]   (rows S..S_pad-1 are 0)
+ *   vt_codes         : e4m3fn [B][H][128][S_pad]   (V transposed; cols S..S_pad-1 are 0)
+ *   q_scale, k_scale : float  [B][H][S_pad/32]     (blocks past ceil(S/32) are 0)
+ *   v_scale          : float  [B][H][128]
+ *   k_mean           : float  [B][H][128]          (0 when smooth_k is off) */
+typedef struct sage_quantized {
+  int8_t* q_codes_dev;
+  int8_t* k_codes_dev;
+  uint8_t* vt_codes_dev;
+  float* q_scale_dev;
+  float* k_scale_dev;
+  float* v_scale_dev;
+  float* k_mean_dev;
+} sage_quantized;
+
+/* ----------------------------------------------------------- size queries -- */
+
+/* Bytes of one quantized bundle for (B, S, H, D), each array starting on a
+ * 256-byte boundary, in the order of sage_quantized's fields. If base_dev is
+ * not NULL, *bundle receives pointers carved from base_dev (which must be
+ * 256-byte aligned and at least *bytes long). Errors: SHAPE, HEAD_DIM,
+ * TOO_LARGE, NULLPTR (bytes NULL, or bundle NULL with base_dev set),
+ * ALIGN (base_dev misaligned). */
+SAGE_API int sage_bundle_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes,
+                     void* base_dev, sage_quantized* bundle);
+
+/* Scratch bytes sage_quantize needs (per-256-token partial key sums in fp64
+ * and partial V maxima). Errors: as sage_bundle_size. */
+SAGE_API int sage_quantize_scratch_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes);
+
+/* Workspace bytes sage_sageattn needs: one bundle plus the quantize scratch. */
+SAGE_API int sage_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes);
+
+/* ------------------------------------------------------------- operations -- */
+
+/* The quantization prologue ("prepare"): optional smooth_k key mean (fp64
+ * sum), INT8 Q/K per 32-token block, e4m3 V per channel, V stored transposed.
+ * q, k, v: BF16 tensors of shape (B, S, H, 128) with the given strides.
+ * scratch_dev: at least sage_quantize_scratch_size bytes, 256-byte aligned;
+ * its contents on entry do not matter and are clobbered.
+ * Three kernels are enqueued: statistics + Q codes, per-head finalisation
+ * (key mean, V scales), then K and V codes.
+ * Errors: NULLPTR, SHAPE, HEAD_DIM, ALIGN, WORKSPACE, TOO_LARGE, ARCH, CUDA. */
+SAGE_API int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k, const sage_bf16_tensor* v,
+                  int64_t B, int64_t S, int64_t H, int64_t D, int smooth_k,
+                  const sage_quantized* out, void* scratch_dev, size_t scratch_bytes,
+                  void* cuda_stream);
+
+/* The attention kernel on a quantized bundle: INT8 QK^T with exact integer
+ * accumulation (run on the tcgen05 tensor cores as fp16 x fp16 -> fp32,
+ * which is exact for |code| <= 127 and 128 channels), dequantization by
+ * s_q * s_k * sm_scale, online fp32 softmax, P -> e4m3, FP8 PV on tcgen05
+ * with fp32 accumulation in tensor memory, V scales in the epilogue.
+ * out: BF16 (B, S, H, 128) at out_dev with element strides (ob, os, oh),
+ * channel stride 1. sm_scale must be finite and > 0.
+ * Errors: NULLPTR, SHAPE, HEAD_DIM, ALIGN, ARG, TOO_LARGE, ARCH, CUDA. */
+SAGE_API int sage_attention(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D,
+                   float sm_scale, void* out_dev, int64_t ob, int64_t os, int64_t oh,
+                   void* cuda_stream);
+
+/* Same contract and result tolerance as sage_attention, computed by a plain
+ * SIMT kernel (integer dot products, one thread per query row). It exists to
+ * cross-check the tensor-core kernel in tests; it is never used as a
+ * fallback. */
+SAGE_API int sage_attention_simt(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D,
+                        float sm_scale, void* out_dev, int64_t ob, int64_t os, int64_t oh,
+                        void* cuda_stream);
+
+/* The sageattn-shaped entry: quantize q, k, v into the workspace, then run
+ * attention into out. Shapes and strides are given in the order of
+ * tensor_layout: "NHD" = [B, S, H, D], "HND" = [B, H, S, D]; strides are in
+ * elements. out has q's shape with out_strides.
+ * sm_scale: NaN selects 1/sqrt(D); otherwise it must be finite and > 0.
+ * Rejected with an error and nothing launched: is_causal != 0 (CAUSAL),
+ * return_lse != 0 (LSE), any dtype other than BF16 (DTYPE), D != 128
+ * (HEAD_DIM), Q/K/V shapes not identical (SHAPE), an unknown layout
+ * (LAYOUT), a channel stride != 1 (LAYOUT), a device other than
+ * compute capability 10.3 (ARCH).
+ * Errors also: NULLPTR, ALIGN, WORKSPACE, ARG, TOO_LARGE, CUDA. */
+SAGE_API int sage_sageattn(const void* q_dev, const void* k_dev, const void* v_dev,
+                  const int64_t q_shape[4], const int64_t k_shape[4], const int64_t v_shape[4],
+                  const int64_t q_strides[4], const int64_t k_strides[4], const int64_t v_strides[4],
+                  int q_dtype, int k_dtype, int v_dtype, const char* tensor_layout,
+                  int is_causal, float sm_scale, int return_lse, int smooth_k,
+                  void* out_dev, const int64_t out_strides[4], int out_dtype,
+                  void* workspace_dev, size_t workspace_bytes, void* cuda_stream);
+
+/* ---------------------------------------------------------- diagnostics -- */
+
+/* Synchronizes cuda_stream, then reads and clears the current device's error
+ * word. Kernels set it (and return early) when a bounded wait on an internal
+ * barrier runs out; they never trap. *code receives SAGE_OK or
+ * SAGE_ERR_DEVICE_TIMEOUT. Returns SAGE_OK, NULLPTR or CUDA. */
+SAGE_API int sage_device_error(void* cuda_stream, int* code);
+
+/* Static description of an error code; never NULL. */
+SAGE_API const char* sage_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGE_H */

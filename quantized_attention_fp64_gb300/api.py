@@ -1,0 +1,235 @@
+"""Python entry points over the C ABI (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; PyTorch is
+used here only to allocate device buffers and to name the current stream.
+If the library is missing the calls raise; there is no other code path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+SAGE_ERR_SHAPE = -5
+SAGE_ERR_LAYOUT = -6
+
+_DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+
+
+class SageError(ValueError):
+    """A call rejected by the library; ``code`` is the SAGE_ERR_* value."""
+
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{message} (sage error {code})")
+        self.code = code
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise SageError(rc, _lib.load().sage_strerror(rc).decode())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    return _DTYPE_CODES.get(t.dtype, 3)
+
+
+def _bsh(shape, layout: str):
+    """(B, S, H, D) from a shape given in ``layout`` order."""
+    if layout == "HND":
+        return shape[0], shape[2], shape[1], shape[3]
+    return shape[0], shape[1], shape[2], shape[3]
+
+
+def _bsh_strides(t: torch.Tensor, layout: str):
+    st = t.stride()
+    if layout == "HND":
+        return st[0], st[2], st[1]
+    return st[0], st[1], st[2]
+
+
+def workspace_size(B: int, S: int, H: int, D: int = 128) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.load().sage_workspace_size(B, S, H, D, ctypes.byref(n)))
+    return n.value
+
+
+def quantize_scratch_size(B: int, S: int, H: int, D: int = 128) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.load().sage_quantize_scratch_size(B, S, H, D, ctypes.byref(n)))
+    return n.value
+
+
+@dataclass
+class QuantizedQKV:
+    """Quantized bundle (views into one device buffer, see sage_quantized)."""
+
+    buffer: torch.Tensor
+    q_codes: torch.Tensor   # int8 [B, H, S_pad, 128]
+    k_codes: torch.Tensor   # int8 [B, H, S_pad, 128]
+    vt_codes: torch.Tensor  # uint8 (e4m3fn) [B, H, 128, S_pad]
+    q_scale: torch.Tensor   # float32 [B, H, S_pad/32]
+    k_scale: torch.Tensor   # float32 [B, H, S_pad/32]
+    v_scale: torch.Tensor   # float32 [B, H, 128]
+    k_mean: torch.Tensor    # float32 [B, H, 128]
+    B: int
+    S: int
+    H: int
+
+    def c_struct(self) -> _lib.Quantized:
+        return _lib.Quantized(*(t.data_ptr() for t in (self.q_codes, self.k_codes, self.vt_codes, self.q_scale,
+                                                       self.k_scale, self.v_scale, self.k_mean)))
+
+
+def alloc_bundle(B: int, S: int, H: int, device) -> QuantizedQKV:
+    lib = _lib.load()
+    n = ctypes.c_size_t(0)
+    _check(lib.sage_bundle_size(B, S, H, 128, ctypes.byref(n), None, None))
+    buf = torch.empty(max(n.value, 256), dtype=torch.uint8, device=device)
+    c = _lib.Quantized()
+    _check(lib.sage_bundle_size(B, S, H, 128, ctypes.byref(n), ctypes.c_void_p(buf.data_ptr()), ctypes.byref(c)))
+    s_pad = -(-S // 128) * 128
+    base = buf.data_ptr()
+
+    def view(ptr, dtype, shape):
+        off = ptr - base
+        count = 1
+        for x in shape:
+            count *= x
+        nbytes = count * torch.tensor([], dtype=dtype).element_size()
+        return buf[off:off + nbytes].view(dtype).view(shape)
+
+    return QuantizedQKV(
+        buffer=buf,
+        q_codes=view(c.q_codes_dev, torch.int8, (B, H, s_pad, 128)),
+        k_codes=view(c.k_codes_dev, torch.int8, (B, H, s_pad, 128)),
+        vt_codes=view(c.vt_codes_dev, torch.uint8, (B, H, 128, s_pad)),
+        q_scale=view(c.q_scale_dev, torch.float32, (B, H, s_pad // 32)),
+        k_scale=view(c.k_scale_dev, torch.float32, (B, H, s_pad // 32)),
+        v_scale=view(c.v_scale_dev, torch.float32, (B, H, 128)),
+        k_mean=view(c.k_mean_dev, torch.float32, (B, H, 128)),
+        B=B, S=S, H=H)
+
+
+def _bf16_tensor(t: torch.Tensor, layout: str) -> _lib.Bf16Tensor:
+    sb, ss, sh = _bsh_strides(t, layout)
+    return _lib.Bf16Tensor(t.data_ptr(), sb, ss, sh)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("expected torch tensors")
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+
+
+def quantize(q, k, v, tensor_layout: str = "NHD", smooth_k: bool = True, out: QuantizedQKV | None = None,
+             scratch: torch.Tensor | None = None) -> QuantizedQKV:
+    """The quantization prologue (sage_quantize) on BF16 tensors."""
+    _require_cuda(q, k, v)
+    if q.dim() != 4 or tuple(q.shape) != tuple(k.shape) or tuple(q.shape) != tuple(v.shape):
+        raise SageError(SAGE_ERR_SHAPE, "q, k and v must have identical 4-d shapes")
+    if tensor_layout not in ("NHD", "HND"):
+        raise SageError(SAGE_ERR_LAYOUT, "tensor_layout must be NHD or HND")
+    if q.stride(3) != 1 or k.stride(3) != 1 or v.stride(3) != 1:
+        raise SageError(SAGE_ERR_LAYOUT, "the channel stride must be 1")
+    B, S, H, D = _bsh(q.shape, tensor_layout)
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise SageError(-3, "inputs and output must be bfloat16")
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        qz = out if out is not None else alloc_bundle(B, S, H, q.device)
+        if scratch is None:
+            scratch = torch.empty(max(quantize_scratch_size(B, S, H, D), 256), dtype=torch.uint8, device=q.device)
+        bundle = qz.c_struct()
+        _check(lib.sage_quantize(ctypes.byref(_bf16_tensor(q, tensor_layout)), ctypes.byref(_bf16_tensor(k, tensor_layout)),
+                                 ctypes.byref(_bf16_tensor(v, tensor_layout)), B, S, H, D, int(bool(smooth_k)),
+                                 ctypes.byref(bundle), ctypes.c_void_p(scratch.data_ptr()), scratch.numel(),
+                                 _stream(q.device)))
+    return qz
+
+
+def _attention(fn_name: str, qz: QuantizedQKV, sm_scale, tensor_layout: str, out):
+    lib = _lib.load()
+    B, S, H = qz.B, qz.S, qz.H
+    device = qz.buffer.device
+    if out is None:
+        shape = (B, H, S, 128) if tensor_layout == "HND" else (B, S, H, 128)
+        out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    scale = (1.0 / math.sqrt(128.0)) if sm_scale is None else float(sm_scale)
+    ob, os_, oh = _bsh_strides(out, tensor_layout)
+    bundle = qz.c_struct()
+    with torch.cuda.device(device):
+        _check(getattr(lib, fn_name)(ctypes.byref(bundle), B, S, H, 128, ctypes.c_float(scale),
+                                     ctypes.c_void_p(out.data_ptr()), ob, os_, oh, _stream(device)))
+    return out
+
+
+def attention(qz: QuantizedQKV, sm_scale=None, tensor_layout: str = "NHD", out=None) -> torch.Tensor:
+    """Tensor-core attention (sage_attention) on a quantized bundle."""
+    return _attention("sage_attention", qz, sm_scale, tensor_layout, out)
+
+
+def attention_simt(qz: QuantizedQKV, sm_scale=None, tensor_layout: str = "NHD", out=None) -> torch.Tensor:
+    """The SIMT cross-check kernel (sage_attention_simt); for tests."""
+    return _attention("sage_attention_simt", qz, sm_scale, tensor_layout, out)
+
+
+def sageattn(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm_scale=None,
+             return_lse: bool = False, smooth_k: bool = True, out=None, workspace=None) -> torch.Tensor:
+    """sageattn(q, k, v, tensor_layout, is_causal, sm_scale, return_lse) through sage_sageattn.
+
+    Unsupported inputs (causal, LSE, non-BF16, head dim != 128, unequal
+    shapes, unknown layout) raise SageError; nothing falls back.
+    """
+    _require_cuda(q, k, v)
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise SageError(SAGE_ERR_SHAPE, "q, k and v must be 4-d")
+    lib = _lib.load()
+    layout = tensor_layout if isinstance(tensor_layout, str) else str(tensor_layout)
+    B, S, H, D = _bsh(q.shape, layout)
+    ws_bytes = ctypes.c_size_t(0)
+    sizes_ok = lib.sage_workspace_size(B, S, H, D, ctypes.byref(ws_bytes)) == 0
+    proceed = (sizes_ok and not is_causal and not return_lse and layout in ("NHD", "HND")
+               and q.dtype == k.dtype == v.dtype == torch.bfloat16
+               and tuple(q.shape) == tuple(k.shape) == tuple(v.shape))
+    with torch.cuda.device(q.device):
+        if proceed and out is None:
+            out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+        if proceed and (workspace is None or workspace.numel() < ws_bytes.value):
+            workspace = torch.empty(max(ws_bytes.value, 256), dtype=torch.uint8, device=q.device)
+        out_ptr = out.data_ptr() if out is not None else None
+        out_strides = out.stride() if out is not None else (0, 0, 0, 1)
+        out_dtype = _dtype_code(out) if out is not None else 0
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_n = workspace.numel() if workspace is not None else 0
+        scale = float("nan") if sm_scale is None else float(sm_scale)
+        rc = lib.sage_sageattn(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+            _lib.I64x4(*q.shape), _lib.I64x4(*k.shape), _lib.I64x4(*v.shape),
+            _lib.I64x4(*q.stride()), _lib.I64x4(*k.stride()), _lib.I64x4(*v.stride()),
+            _dtype_code(q), _dtype_code(k), _dtype_code(v), layout.encode(), int(bool(is_causal)),
+            ctypes.c_float(scale), int(bool(return_lse)), int(bool(smooth_k)),
+            ctypes.c_void_p(out_ptr), _lib.I64x4(*out_strides), out_dtype,
+            ctypes.c_void_p(ws_ptr), ws_n, _stream(q.device))
+    _check(rc)
+    return out
+
+
+def device_error(device=None) -> int:
+    """Synchronizes the current stream and returns (and clears) the device error word."""
+    lib = _lib.load()
+    code = ctypes.c_int(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib.sage_device_error(_stream(dev), ctypes.byref(code)))
+    return code.value

@@ -1,0 +1,335 @@
+// C ABI of the library: argument validation, buffer layout, dispatch.
+//
+// Entry-point contract: "aiter-sage-attention: SageAttention for AMD RDNA4
+// (gfx1201) #1222", section "What I have so far" -- sageattn(q, k, v,
+// tensor_layout, is_causal, sm_scale, return_lse) rejects causal, LSE,
+// non-BF16, head dim other than 128 and unequal Q/K/V shapes with an error
+// and never falls back. Everything is validated on the host before any work
+// is enqueued.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sage.h"
+#include "common.cuh"
+
+namespace sage {
+namespace {
+
+// Set by kernels that give up a bounded wait; read and cleared by
+// sage_device_error. Host code reaches it through cudaGetSymbolAddress.
+__device__ int g_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 wrong architecture
+
+// Largest accepted sizes: every index stays far inside int64, the grids stay
+// inside CUDA's limits (H and B are grid dimensions of the prologue) and the
+// 2-D and 3-D tensor maps of the attention kernel keep 32-bit coordinates.
+constexpr int64_t kMaxBH = 65535;
+constexpr int64_t kMaxS = int64_t(1) << 31;
+constexpr int64_t kMaxElems = int64_t(1) << 44;
+
+int check_device(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SAGE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SAGE_ERR_CUDA;
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_arch_ok[dev] < 0) return SAGE_ERR_ARCH;
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return SAGE_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *dev_out = dev;
+  return SAGE_OK;
+}
+
+int check_sizes(int64_t B, int64_t S, int64_t H, int64_t D) {
+  if (B < 0 || S < 0 || H < 0 || D < 0) return SAGE_ERR_SHAPE;
+  if (D != kHeadDim) return SAGE_ERR_HEAD_DIM;
+  if (B > kMaxBH || H > kMaxBH || S > kMaxS) return SAGE_ERR_TOO_LARGE;
+  if (B * H > kMaxBH * 16) return SAGE_ERR_TOO_LARGE;
+  if (B * H * padded_len(S) > kMaxElems / kHeadDim) return SAGE_ERR_TOO_LARGE;
+  return SAGE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool stride_ok(int64_t s) { return s % 8 == 0; }
+
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+struct BundleLayout {
+  size_t off[7];
+  size_t total;
+};
+
+BundleLayout bundle_layout(int64_t B, int64_t S, int64_t H) {
+  const size_t bh = static_cast<size_t>(B * H);
+  const size_t sp = static_cast<size_t>(padded_len(S));
+  const size_t sizes[7] = {bh * sp * kHeadDim, bh * sp * kHeadDim, bh * sp * kHeadDim,
+                           bh * (sp / kQKBlock) * 4, bh * (sp / kQKBlock) * 4, bh * kHeadDim * 4,
+                           bh * kHeadDim * 4};
+  BundleLayout l;
+  size_t o = 0;
+  for (int i = 0; i < 7; ++i) {
+    l.off[i] = o;
+    o += round256(sizes[i]);
+  }
+  l.total = o;
+  return l;
+}
+
+Bundle carve(void* base, const BundleLayout& l) {
+  char* c = static_cast<char*>(base);
+  Bundle b;
+  b.q_codes = reinterpret_cast<int8_t*>(c + l.off[0]);
+  b.k_codes = reinterpret_cast<int8_t*>(c + l.off[1]);
+  b.vt_codes = reinterpret_cast<uint8_t*>(c + l.off[2]);
+  b.q_scale = reinterpret_cast<float*>(c + l.off[3]);
+  b.k_scale = reinterpret_cast<float*>(c + l.off[4]);
+  b.v_scale = reinterpret_cast<float*>(c + l.off[5]);
+  b.k_mean = reinterpret_cast<float*>(c + l.off[6]);
+  return b;
+}
+
+int check_bundle(const sage_quantized* in, bool need_mean) {
+  if (in == nullptr) return SAGE_ERR_NULLPTR;
+  const void* ptrs[7] = {in->q_codes_dev, in->k_codes_dev, in->vt_codes_dev, in->q_scale_dev,
+                         in->k_scale_dev, in->v_scale_dev, in->k_mean_dev};
+  for (int i = 0; i < 7; ++i) {
+    if (i == 6 && !need_mean) continue;
+    if (ptrs[i] == nullptr) return SAGE_ERR_NULLPTR;
+    if (!aligned16(ptrs[i])) return SAGE_ERR_ALIGN;
+  }
+  return SAGE_OK;
+}
+
+Bundle to_bundle(const sage_quantized* in) {
+  Bundle b;
+  b.q_codes = in->q_codes_dev;
+  b.k_codes = in->k_codes_dev;
+  b.vt_codes = in->vt_codes_dev;
+  b.q_scale = in->q_scale_dev;
+  b.k_scale = in->k_scale_dev;
+  b.v_scale = in->v_scale_dev;
+  b.k_mean = in->k_mean_dev;
+  return b;
+}
+
+int check_bf16_in(const sage_bf16_tensor* t) {
+  if (t == nullptr || t->ptr_dev == nullptr) return SAGE_ERR_NULLPTR;
+  if (!aligned16(t->ptr_dev)) return SAGE_ERR_ALIGN;
+  if (!stride_ok(t->stride_b) || !stride_ok(t->stride_s) || !stride_ok(t->stride_h)) return SAGE_ERR_ALIGN;
+  return SAGE_OK;
+}
+
+int check_out(const void* out, int64_t ob, int64_t os, int64_t oh) {
+  if (out == nullptr) return SAGE_ERR_NULLPTR;
+  if (!aligned16(out) || !stride_ok(ob) || !stride_ok(os) || !stride_ok(oh)) return SAGE_ERR_ALIGN;
+  return SAGE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA; }
+
+typedef cudaError_t (*AttnLaunch)(const Bundle&, int64_t, int64_t, int64_t, float, const Out&, int*, cudaStream_t);
+
+cudaError_t simt_adapter(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm, const Out& o, int*,
+                         cudaStream_t st) {
+  return launch_attention_simt(in, B, S, H, sm, o, st);
+}
+
+int attention_common(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
+                     void* out_dev, int64_t ob, int64_t os, int64_t oh, void* stream, AttnLaunch launch) {
+  int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  if ((rc = check_bundle(in, false)) != SAGE_OK) return rc;
+  if ((rc = check_out(out_dev, ob, os, oh)) != SAGE_OK) return rc;
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.0f)) return SAGE_ERR_ARG;
+  int dev = 0;
+  if ((rc = check_device(&dev)) != SAGE_OK) return rc;
+  if (B == 0 || H == 0 || S == 0) return SAGE_OK;
+  Out o{static_cast<uint16_t*>(out_dev), ob, os, oh};
+  return cuda_status(launch(to_bundle(in), B, S, H, sm_scale, o, g_err_ptr[dev], static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+}  // namespace sage
+
+using namespace sage;
+
+extern "C" {
+
+int sage_bundle_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes, void* base_dev,
+                     sage_quantized* bundle) {
+  if (bytes == nullptr) return SAGE_ERR_NULLPTR;
+  const int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  const BundleLayout l = bundle_layout(B, S, H);
+  *bytes = l.total;
+  if (base_dev != nullptr) {
+    if (bundle == nullptr) return SAGE_ERR_NULLPTR;
+    if ((reinterpret_cast<uintptr_t>(base_dev) & 255u) != 0) return SAGE_ERR_ALIGN;
+    const Bundle b = carve(base_dev, l);
+    bundle->q_codes_dev = b.q_codes;
+    bundle->k_codes_dev = b.k_codes;
+    bundle->vt_codes_dev = b.vt_codes;
+    bundle->q_scale_dev = b.q_scale;
+    bundle->k_scale_dev = b.k_scale;
+    bundle->v_scale_dev = b.v_scale;
+    bundle->k_mean_dev = b.k_mean;
+  }
+  return SAGE_OK;
+}
+
+int sage_quantize_scratch_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes) {
+  if (bytes == nullptr) return SAGE_ERR_NULLPTR;
+  const int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  *bytes = prologue_scratch_bytes(B, S, H);
+  return SAGE_OK;
+}
+
+int sage_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes) {
+  if (bytes == nullptr) return SAGE_ERR_NULLPTR;
+  const int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  *bytes = bundle_layout(B, S, H).total + prologue_scratch_bytes(B, S, H);
+  return SAGE_OK;
+}
+
+int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k, const sage_bf16_tensor* v, int64_t B,
+                  int64_t S, int64_t H, int64_t D, int smooth_k, const sage_quantized* out, void* scratch_dev,
+                  size_t scratch_bytes, void* cuda_stream) {
+  int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  if ((rc = check_bf16_in(q)) != SAGE_OK || (rc = check_bf16_in(k)) != SAGE_OK || (rc = check_bf16_in(v)) != SAGE_OK)
+    return rc;
+  if ((rc = check_bundle(out, true)) != SAGE_OK) return rc;
+  if (scratch_dev == nullptr) return SAGE_ERR_NULLPTR;
+  if ((reinterpret_cast<uintptr_t>(scratch_dev) & 255u) != 0) return SAGE_ERR_ALIGN;
+  if (scratch_bytes < prologue_scratch_bytes(B, S, H)) return SAGE_ERR_WORKSPACE;
+  int dev = 0;
+  if ((rc = check_device(&dev)) != SAGE_OK) return rc;
+  if (B == 0 || H == 0 || S == 0) return SAGE_OK;
+  const Bf16In qi{static_cast<const uint16_t*>(q->ptr_dev), q->stride_b, q->stride_s, q->stride_h};
+  const Bf16In ki{static_cast<const uint16_t*>(k->ptr_dev), k->stride_b, k->stride_s, k->stride_h};
+  const Bf16In vi{static_cast<const uint16_t*>(v->ptr_dev), v->stride_b, v->stride_s, v->stride_h};
+  return cuda_status(launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, to_bundle(out), scratch_dev,
+                                     static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int sage_attention(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
+                   void* out_dev, int64_t ob, int64_t os, int64_t oh, void* cuda_stream) {
+  return attention_common(in, B, S, H, D, sm_scale, out_dev, ob, os, oh, cuda_stream, launch_attention_tc);
+}
+
+int sage_attention_simt(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
+                        void* out_dev, int64_t ob, int64_t os, int64_t oh, void* cuda_stream) {
+  return attention_common(in, B, S, H, D, sm_scale, out_dev, ob, os, oh, cuda_stream, simt_adapter);
+}
+
+int sage_sageattn(const void* q_dev, const void* k_dev, const void* v_dev, const int64_t q_shape[4],
+                  const int64_t k_shape[4], const int64_t v_shape[4], const int64_t q_strides[4],
+                  const int64_t k_strides[4], const int64_t v_strides[4], int q_dtype, int k_dtype, int v_dtype,
+                  const char* tensor_layout, int is_causal, float sm_scale, int return_lse, int smooth_k,
+                  void* out_dev, const int64_t out_strides[4], int out_dtype, void* workspace_dev,
+                  size_t workspace_bytes, void* cuda_stream) {
+  // The contract's rejections come first, in the order the pages list them.
+  if (is_causal) return SAGE_ERR_CAUSAL;
+  if (return_lse) return SAGE_ERR_LSE;
+  if (q_dtype != SAGE_DTYPE_BF16 || k_dtype != SAGE_DTYPE_BF16 || v_dtype != SAGE_DTYPE_BF16 ||
+      out_dtype != SAGE_DTYPE_BF16)
+    return SAGE_ERR_DTYPE;
+  if (q_shape == nullptr || k_shape == nullptr || v_shape == nullptr || q_strides == nullptr ||
+      k_strides == nullptr || v_strides == nullptr || out_strides == nullptr || tensor_layout == nullptr)
+    return SAGE_ERR_NULLPTR;
+  int is_nhd;
+  if (std::strcmp(tensor_layout, "NHD") == 0) is_nhd = 1;
+  else if (std::strcmp(tensor_layout, "HND") == 0) is_nhd = 0;
+  else return SAGE_ERR_LAYOUT;
+  // axis positions of (b, s, h, d) in the given layout
+  const int ax_s = is_nhd ? 1 : 2, ax_h = is_nhd ? 2 : 1;
+  const int64_t B = q_shape[0], S = q_shape[ax_s], H = q_shape[ax_h], D = q_shape[3];
+  if (D != kHeadDim && D >= 0) return SAGE_ERR_HEAD_DIM;
+  for (int i = 0; i < 4; ++i)
+    if (k_shape[i] != q_shape[i] || v_shape[i] != q_shape[i]) return SAGE_ERR_SHAPE;
+  int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  const int64_t* st[4] = {q_strides, k_strides, v_strides, out_strides};
+  for (int i = 0; i < 4; ++i)
+    if (st[i][3] != 1) return SAGE_ERR_LAYOUT;
+  if (!(std::isnan(sm_scale) || (std::isfinite(sm_scale) && sm_scale > 0.0f))) return SAGE_ERR_ARG;
+  const float scale = std::isnan(sm_scale) ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) : sm_scale;
+  const sage_bf16_tensor qt{q_dev, q_strides[0], q_strides[ax_s], q_strides[ax_h]};
+  const sage_bf16_tensor kt{k_dev, k_strides[0], k_strides[ax_s], k_strides[ax_h]};
+  const sage_bf16_tensor vt{v_dev, v_strides[0], v_strides[ax_s], v_strides[ax_h]};
+  if ((rc = check_bf16_in(&qt)) != SAGE_OK || (rc = check_bf16_in(&kt)) != SAGE_OK ||
+      (rc = check_bf16_in(&vt)) != SAGE_OK)
+    return rc;
+  if ((rc = check_out(out_dev, out_strides[0], out_strides[ax_s], out_strides[ax_h])) != SAGE_OK) return rc;
+  if (workspace_dev == nullptr) return SAGE_ERR_NULLPTR;
+  if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return SAGE_ERR_ALIGN;
+  const BundleLayout bl = bundle_layout(B, S, H);
+  const size_t scratch = prologue_scratch_bytes(B, S, H);
+  if (workspace_bytes < bl.total + scratch) return SAGE_ERR_WORKSPACE;
+  int dev = 0;
+  if ((rc = check_device(&dev)) != SAGE_OK) return rc;
+  if (B == 0 || H == 0 || S == 0) return SAGE_OK;
+  const Bundle bundle = carve(workspace_dev, bl);
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  const Bf16In qi{static_cast<const uint16_t*>(q_dev), qt.stride_b, qt.stride_s, qt.stride_h};
+  const Bf16In ki{static_cast<const uint16_t*>(k_dev), kt.stride_b, kt.stride_s, kt.stride_h};
+  const Bf16In vi{static_cast<const uint16_t*>(v_dev), vt.stride_b, vt.stride_s, vt.stride_h};
+  if ((rc = cuda_status(launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, bundle,
+                                        static_cast<char*>(workspace_dev) + bl.total, stream))) != SAGE_OK)
+    return rc;
+  const Out o{static_cast<uint16_t*>(out_dev), out_strides[0], out_strides[ax_s], out_strides[ax_h]};
+  return cuda_status(launch_attention_tc(bundle, B, S, H, scale, o, g_err_ptr[dev], stream));
+}
+
+int sage_device_error(void* cuda_stream, int* code) {
+  if (code == nullptr) return SAGE_ERR_NULLPTR;
+  int dev = 0;
+  int rc = check_device(&dev);
+  if (rc != SAGE_OK) return rc;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SAGE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, g_err_ptr[dev], sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SAGE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(g_err_ptr[dev], &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SAGE_ERR_CUDA;
+  *code = v == 0 ? SAGE_OK : SAGE_ERR_DEVICE_TIMEOUT;
+  return SAGE_OK;
+}
+
+const char* sage_strerror(int code) {
+  switch (code) {
+    case SAGE_OK: return "success";
+    case SAGE_ERR_CAUSAL: return "is_causal is not supported (non-causal attention only)";
+    case SAGE_ERR_LSE: return "return_lse is not supported";
+    case SAGE_ERR_DTYPE: return "inputs and output must be bfloat16";
+    case SAGE_ERR_HEAD_DIM: return "head dimension must be 128";
+    case SAGE_ERR_SHAPE: return "q, k and v must have identical, non-negative shapes";
+    case SAGE_ERR_LAYOUT: return "tensor_layout must be \"NHD\" or \"HND\" with a unit channel stride";
+    case SAGE_ERR_ALIGN: return "pointers must be 16-byte aligned and strides multiples of 8 elements";
+    case SAGE_ERR_NULLPTR: return "a required pointer is NULL";
+    case SAGE_ERR_WORKSPACE: return "workspace or scratch buffer is too small";
+    case SAGE_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103)";
+    case SAGE_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case SAGE_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on an internal barrier";
+    case SAGE_ERR_ARG: return "invalid argument (sm_scale must be finite and positive)";
+    case SAGE_ERR_TOO_LARGE: return "sizes exceed the library's limits";
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Shared definitions for the CUDA side of the library (kernels and C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace sage {
+
+constexpr int kHeadDim = 128;     // the only supported head dimension
+constexpr int kQKBlock = 32;      // tokens per Q/K scale block ("per 32-row block")
+constexpr int kKeyTile = 128;     // keys per online-softmax step; S is padded to this
+constexpr int kGroup = 256;       // tokens per prologue CTA (8 warps x 32 tokens)
+constexpr float kInt8Max = 127.0f;
+constexpr float kE4M3Max = 448.0f;  // largest finite e4m3fn magnitude
+constexpr float kPScale = 448.0f;   // p in [0,1] is stored as e4m3(448 p)
+
+__host__ __device__ inline int64_t padded_len(int64_t s) { return (s + kKeyTile - 1) / kKeyTile * kKeyTile; }
+__host__ __device__ inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Device error word values (written by kernels that give up a bounded wait).
+constexpr int kDevErrTimeout = 1;
+
+// One BF16 input: element (b, s, h, d) at p[b*sb + s*ss + h*sh + d].
+struct Bf16In {
+  const uint16_t* p;
+  int64_t sb, ss, sh;
+};
+
+// The quantized bundle (device pointers), mirroring sage_quantized.
+struct Bundle {
+  int8_t* q_codes;
+  int8_t* k_codes;
+  uint8_t* vt_codes;
+  float* q_scale;
+  float* k_scale;
+  float* v_scale;
+  float* k_mean;
+};
+
+// BF16 output: element (b, s, h, d) at p[b*sb + s*ss + h*sh + d].
+struct Out {
+  uint16_t* p;
+  int64_t sb, ss, sh;
+};
+
+// Launchers implemented by the kernel translation units. Each enqueues on
+// `stream` and returns the launch status (cudaGetLastError).
+cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, int64_t B, int64_t S,
+                            int64_t H, bool smooth_k, const Bundle& out, void* scratch,
+                            cudaStream_t stream);
+size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H);
+
+cudaError_t launch_attention_simt(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale,
+                                  const Out& out, cudaStream_t stream);
+
+cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale,
+                                const Out& out, int* dev_err, cudaStream_t stream);
+
+}  // namespace sage

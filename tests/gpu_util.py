@@ -1,0 +1,64 @@
+"""Helpers shared by the GPU parity tests (comparison and conversion only)."""
+
+import numpy as np
+import torch
+
+from oracle.tensors import attention_from_codes, exact_head, quantize_tensors
+
+ATOL_MAX = 2e-2    # max |gpu - emulation| on bf16 outputs
+ATOL_MEAN = 2e-3   # mean |gpu - emulation|
+COS_MIN = 0.999    # cosine against exact fp64 attention
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy()
+
+
+def bundle_np(qz):
+    return dict(q_codes=qz.q_codes.cpu().numpy(), k_codes=qz.k_codes.cpu().numpy(),
+                vt_codes=qz.vt_codes.cpu().numpy(), q_scale=qz.q_scale.cpu().numpy(),
+                k_scale=qz.k_scale.cpu().numpy(), v_scale=qz.v_scale.cpu().numpy(),
+                k_mean=qz.k_mean.cpu().numpy())
+
+
+def assert_bundles_equal(got: dict, ref: dict, heads=None):
+    for key in ("q_codes", "k_codes", "vt_codes", "q_scale", "k_scale", "v_scale", "k_mean"):
+        a, b = got[key], ref[key]
+        if heads is not None:
+            a = np.stack([a[bb, hh] for bb, hh in heads])
+            b = np.stack([b[bb, hh] for bb, hh in heads])
+        if a.dtype == np.float32:
+            a, b = a.view(np.uint32), b.view(np.uint32)
+        bad = np.argwhere(a != b)
+        assert bad.size == 0, f"{key}: {len(bad)} mismatches, first at {bad[:5].tolist()}: " \
+                              f"gpu {a[tuple(bad[0])]:#x} oracle {b[tuple(bad[0])]:#x}"
+
+
+def head_out(out: np.ndarray, layout: str, b: int, h: int) -> np.ndarray:
+    return out[b, :, h, :] if layout == "NHD" else out[b, h, :, :]
+
+
+def cosine(a, b) -> float:
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
+
+
+def check_attention(out_gpu: np.ndarray, q, k, v, layout: str, qz_ref: dict, sm_scale: float, heads, rows=None):
+    """Compares a GPU attention output with the oracle's emulation (max/mean
+    abs) and exact attention (cosine) on the given heads and query rows."""
+    s_len = q.shape[1] if layout == "NHD" else q.shape[2]
+    errs, gpu_all, exact_all = [], [], []
+    for b, h in heads:
+        emu = attention_from_codes(qz_ref, s_len, sm_scale, b, h, rows=rows)
+        got = head_out(out_gpu, layout, b, h)
+        got = got if rows is None else got[rows]
+        errs.append(np.abs(got.astype(np.float64) - emu))
+        gpu_all.append(got)
+        exact_all.append(exact_head(q, k, v, layout, sm_scale, b, h, rows=rows))
+    err = np.concatenate([e.ravel() for e in errs])
+    cos = cosine(np.concatenate([g.ravel() for g in gpu_all]), np.concatenate([e.ravel() for e in exact_all]))
+    assert err.max() <= ATOL_MAX, f"max abs err {err.max()}"
+    assert err.mean() <= ATOL_MEAN, f"mean abs err {err.mean()}"
+    assert cos >= COS_MIN, f"cosine vs exact {cos}"
+    return err.max(), err.mean(), cos

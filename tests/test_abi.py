@@ -1,0 +1,140 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, answers size queries, and rejects invalid calls before it
+touches the device (every case here has an argument the host validation
+refuses, so nothing is ever launched)."""
+
+import ctypes
+import math
+
+import pytest
+import torch
+
+from quantized_attention_fp64_gb300 import _build, _lib
+from quantized_attention_fp64_gb300.api import SageError, sageattn
+
+OK, CAUSAL, LSE, DTYPE, HEAD_DIM, SHAPE, LAYOUT, ALIGN, NULLPTR, WORKSPACE = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+ARG, TOO_LARGE = -13, -14
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _lib.header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_covers_codes(lib):
+    for code in range(0, -15, -1):
+        msg = lib.sage_strerror(code)
+        assert msg and b"unknown" not in msg
+    assert b"unknown" in lib.sage_strerror(-99)
+
+
+def _sizes(lib, fn, *args):
+    n = ctypes.c_size_t(0)
+    rc = getattr(lib, fn)(*args, ctypes.byref(n))
+    return rc, n.value
+
+
+def test_size_queries(lib):
+    B, S, H = 1, 16384, 28
+    rc, ws = _sizes(lib, "sage_workspace_size", B, S, H, 128)
+    assert rc == OK
+    rc, sc = _sizes(lib, "sage_quantize_scratch_size", B, S, H, 128)
+    assert rc == OK
+    n = ctypes.c_size_t(0)
+    assert lib.sage_bundle_size(B, S, H, 128, ctypes.byref(n), None, None) == OK
+    # codes: 3 x B*H*S_pad*128 bytes; scales and means are small
+    assert n.value >= 3 * B * H * S * 128
+    assert ws == n.value + sc
+    # scratch: fp64 + fp32 per (head, 256-token group, channel), 256-aligned
+    assert sc == 28 * 64 * 128 * 8 + 28 * 64 * 128 * 4
+    assert _sizes(lib, "sage_workspace_size", 1, 100, 2, 64)[0] == HEAD_DIM
+    assert _sizes(lib, "sage_workspace_size", -1, 100, 2, 128)[0] == SHAPE
+    assert _sizes(lib, "sage_workspace_size", 1, 2 ** 40, 2, 128)[0] == TOO_LARGE
+    assert _sizes(lib, "sage_workspace_size", 0, 0, 0, 128) == (OK, 0) or _sizes(lib, "sage_workspace_size", 0, 0, 0, 128)[0] == OK
+    assert lib.sage_workspace_size(1, 1, 1, 128, None) == NULLPTR
+
+
+def test_bundle_carve_alignment(lib):
+    n = ctypes.c_size_t(0)
+    c = _lib.Quantized()
+    assert lib.sage_bundle_size(2, 1000, 3, 128, ctypes.byref(n), ctypes.c_void_p(0x100000), ctypes.byref(c)) == OK
+    ptrs = [c.q_codes_dev, c.k_codes_dev, c.vt_codes_dev, c.q_scale_dev, c.k_scale_dev, c.v_scale_dev, c.k_mean_dev]
+    assert ptrs[0] == 0x100000 and all(p % 256 == 0 for p in ptrs)
+    assert ptrs == sorted(ptrs) and ptrs[-1] + 2 * 3 * 128 * 4 <= 0x100000 + n.value
+    assert lib.sage_bundle_size(2, 1000, 3, 128, ctypes.byref(n), ctypes.c_void_p(0x100010), ctypes.byref(c)) == ALIGN
+
+
+def _call_sageattn(lib, **over):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, shape=(1, 256, 2, 128), kshape=None, vshape=None,
+             strides=(256 * 2 * 128, 2 * 128, 128, 1), dt=0, kdt=0, vdt=0, layout=b"NHD", causal=0, sm=float("nan"),
+             lse=0, smooth=1, out=0x40000, ostrides=None, odt=0, ws=0x50000, wsn=1 << 40)
+    a.update(over)
+    I = _lib.I64x4
+    return lib.sage_sageattn(ctypes.c_void_p(a["q"]), ctypes.c_void_p(a["k"]), ctypes.c_void_p(a["v"]),
+                             I(*a["shape"]), I(*(a["kshape"] or a["shape"])), I(*(a["vshape"] or a["shape"])),
+                             I(*a["strides"]), I(*a["strides"]), I(*a["strides"]), a["dt"], a["kdt"], a["vdt"],
+                             a["layout"], a["causal"], ctypes.c_float(a["sm"]), a["lse"], a["smooth"],
+                             ctypes.c_void_p(a["out"]), I(*(a["ostrides"] or a["strides"])), a["odt"],
+                             ctypes.c_void_p(a["ws"]), a["wsn"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(causal=1), CAUSAL),
+    (dict(lse=1), LSE),
+    (dict(causal=1, lse=1), CAUSAL),
+    (dict(dt=1), DTYPE), (dict(kdt=2), DTYPE), (dict(vdt=3), DTYPE), (dict(odt=1), DTYPE),
+    (dict(shape=(1, 256, 2, 64)), HEAD_DIM),
+    (dict(kshape=(1, 255, 2, 128)), SHAPE),
+    (dict(vshape=(1, 256, 3, 128)), SHAPE),
+    (dict(layout=b"BSHD"), LAYOUT),
+    (dict(strides=(65536, 256, 128, 2)), LAYOUT),
+    (dict(q=0x10008), ALIGN),
+    (dict(strides=(65536, 260, 128, 1)), ALIGN),
+    (dict(out=0x40004), ALIGN),
+    (dict(q=0), NULLPTR), (dict(out=0), NULLPTR), (dict(ws=0), NULLPTR),
+    (dict(ws=0x50010), ALIGN),
+    (dict(wsn=1000), WORKSPACE),
+    (dict(sm=-1.0), ARG), (dict(sm=float("inf")), ARG), (dict(sm=0.0), ARG),
+    (dict(shape=(1, 2 ** 40, 2, 128), strides=(2 ** 48, 256, 128, 1)), TOO_LARGE),
+])
+def test_sageattn_rejections(lib, over, code):
+    assert _call_sageattn(lib, **over) == code
+
+
+def test_quantize_and_attention_rejections(lib):
+    t = _lib.Bf16Tensor(0x10000, 65536, 256, 128)
+    bad = _lib.Bf16Tensor(0x10002, 65536, 256, 128)
+    nul = _lib.Bf16Tensor(0, 65536, 256, 128)
+    qz = _lib.Quantized(0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000)
+    r = ctypes.byref
+    assert lib.sage_quantize(r(t), r(t), r(t), 1, 256, 2, 64, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == HEAD_DIM
+    assert lib.sage_quantize(r(bad), r(t), r(t), 1, 256, 2, 128, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == ALIGN
+    assert lib.sage_quantize(r(t), r(nul), r(t), 1, 256, 2, 128, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == NULLPTR
+    assert lib.sage_quantize(r(t), r(t), r(t), 1, 256, 2, 128, 1, r(qz), ctypes.c_void_p(0x800000), 16, None) == WORKSPACE
+    assert lib.sage_quantize(r(t), r(t), r(t), 1, 256, 2, 128, 1, r(qz), None, 1 << 30, None) == NULLPTR
+    qz_bad = _lib.Quantized(0x100000, 0x200004, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000)
+    out = ctypes.c_void_p(0x900000)
+    for fn in ("sage_attention", "sage_attention_simt"):
+        f = getattr(lib, fn)
+        assert f(r(qz), 1, 256, 2, 128, ctypes.c_float(-0.1), out, 65536, 256, 128, None) == ARG
+        assert f(r(qz), 1, 256, 2, 128, ctypes.c_float(math.nan), out, 65536, 256, 128, None) == ARG
+        assert f(r(qz_bad), 1, 256, 2, 128, ctypes.c_float(0.1), out, 65536, 256, 128, None) == ALIGN
+        assert f(r(qz), 1, 256, 2, 100, ctypes.c_float(0.1), out, 65536, 256, 128, None) == HEAD_DIM
+        assert f(None, 1, 256, 2, 128, ctypes.c_float(0.1), out, 65536, 256, 128, None) == NULLPTR
+        assert f(r(qz), 1, 256, 2, 128, ctypes.c_float(0.1), None, 65536, 256, 128, None) == NULLPTR
+        assert f(r(qz), 1, 256, 2, 128, ctypes.c_float(0.1), out, 65536, 252, 128, None) == ALIGN
+
+
+def test_python_binding_rejects_host_tensors():
+    q = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        sageattn(q, q, q)
+    assert issubclass(SageError, ValueError)

@@ -1,0 +1,78 @@
+"""GPU prologue against the oracle: INT8 Q/K codes, e4m3 V codes, every scale
+and the key mean must match bit for bit."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_bundles_equal, bundle_np, to_np
+from oracle.tensors import quantize_tensors
+from quantized_attention_fp64_gb300 import quantize
+from quantized_attention_fp64_gb300.workloads import WORKLOADS, custom, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q, k, v, layout, smooth, heads=None):
+    qz = quantize(q, k, v, layout, smooth)
+    torch.cuda.synchronize()
+    ref = quantize_tensors(to_np(q), to_np(k), to_np(v), layout, smooth, heads=heads)
+    assert_bundles_equal(bundle_np(qz), ref, heads=heads)
+
+
+@pytest.mark.parametrize("name,smooth,layout", [
+    ("B1_H2_S256", False, "NHD"), ("B1_H2_S256", True, "NHD"),
+    ("B2_H8_S1024", True, "NHD"), ("B2_H8_S1024", False, "NHD"), ("B2_H8_S1024", True, "HND"),
+    ("B1_H28_S4096", True, "NHD"),
+])
+def test_prologue_configs(sage_lib, name, smooth, layout):
+    q, k, v = make_qkv(WORKLOADS[name], "cuda", layout)
+    _run(q, k, v, layout, smooth)
+
+
+@pytest.mark.parametrize("s_len", [1, 31, 33, 129, 255, 257, 1000, 4097])
+def test_prologue_ragged_lengths(sage_lib, s_len):
+    w = custom(2, 3, s_len, seed_index=200 + s_len, k_offset_std=2.0)
+    q, k, v = make_qkv(w, "cuda")
+    _run(q, k, v, "NHD", True)
+
+
+def test_prologue_full_video_size(sage_lib):
+    q, k, v = make_qkv(WORKLOADS["B1_H28_S16384"], "cuda")
+    _run(q, k, v, "NHD", True)
+
+
+def test_prologue_long_sequence_sampled_heads(sage_lib):
+    # Past 100k tokens (the length that used to need 64-bit offsets); the
+    # oracle checks three heads in full.
+    q, k, v = make_qkv(WORKLOADS["B1_H28_S131072"], "cuda")
+    _run(q, k, v, "NHD", True, heads=[(0, 0), (0, 13), (0, 27)])
+
+
+def test_prologue_edge_values(sage_lib):
+    """Zero blocks and channels, negative zeros, bf16 subnormals, exact .5
+    ties of x/s, a key chunk whose fp64 sum rounds (forcing the exact fp64
+    path) and huge magnitudes."""
+    rng = np.random.default_rng(5)
+    S, H = 300, 2
+    q = rng.standard_normal((1, S, H, 128)).astype(np.float32)
+    k = rng.standard_normal((1, S, H, 128)).astype(np.float32) + 3.0
+    v = rng.standard_normal((1, S, H, 128)).astype(np.float32)
+    q[0, 32:64, 0] = 0.0                       # zero Q block
+    q[0, 64:96, 0] = -0.0                      # negative-zero Q block
+    q[0, 96:128, 0] = 1e-39                    # subnormal bf16 block: s is subnormal
+    q[0, 96, 0, 5] = 3e-39
+    q[0, 128:160, 0] = np.round(rng.uniform(-127, 127, (32, 128)) * 2) / 2   # x/s ties
+    q[0, 128, 0, 0] = 127.0
+    k[0, 0, 1, 7], k[0, 1, 1, 7], k[0, 2, 1, 7] = 2.0 ** 60, 1.0, -(2.0 ** 60)   # rounding fp64 chunk sum
+    k[0, 40:72, 1, 9] = 1e-38                  # tiny values beside large ones
+    k[0, 40, 1, 9] = 1e30
+    v[0, :, 1, 3] = 0.0                        # zero V channel
+    v[0, :, 1, 4] = -0.0                       # negative-zero V channel
+    v[0, :, 0, 6] = 1e-39                      # subnormal V channel: s_v subnormal
+    v[0, 7, 0, 6] = -2e-39
+    v[0, 10, 0, 8] = 1e35                      # one huge value dominates its channel
+    dev = torch.device("cuda")
+    qt, kt, vt = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (q, k, v))
+    for smooth in (True, False):
+        _run(qt, kt, vt, "NHD", smooth)
