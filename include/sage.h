@@ -152,6 +152,30 @@ SAGE_API int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k,
                   const sage_quantized* out, void* scratch_dev, size_t scratch_bytes,
                   void* cuda_stream);
 
+/* sage_quantize for callers that cannot allocate device memory. Some callers
+ * cannot call cudaMalloc or any allocating routine (code running under a
+ * memory budget fixed up front, plug-ins handed only the tensors they read and
+ * write, hosts whose allocator must not be entered from the calling thread),
+ * so they cannot provide sage_quantize's scratch buffer. This entry point
+ * takes the same inputs and outputs and no scratch: the prologue's partial
+ * sums go to a 32 MiB device array built into the library, which every GPU
+ * that loads the library holds until the process exits. The web pages this
+ * library follows have no counterpart to this entry point.
+ * Limit: the problem must need at most 32 MiB of prologue scratch, i.e.
+ * B * H * ceil(S / 256) * 128 * 12 bytes (each part rounded up to 256 bytes)
+ * <= 32 MiB, about 21 800 (head, 256-token group) pairs; larger problems are
+ * rejected with SAGE_ERR_WORKSPACE and nothing is launched.
+ * The first call on each device looks up the array's device address with
+ * cudaGetSymbolAddress; make that first call before any stream capture.
+ * All calls share the array and it keeps the last call's contents (nothing in
+ * it needs to start at zero); calls whose work overlaps on the GPU race on it,
+ * so order them on one stream. Allocates nothing; results are identical to
+ * sage_quantize's.
+ * Errors: NULLPTR, SHAPE, HEAD_DIM, ALIGN, WORKSPACE, TOO_LARGE, ARCH, CUDA. */
+SAGE_API int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_tensor* k,
+                                   const sage_bf16_tensor* v, int64_t B, int64_t S, int64_t H, int64_t D,
+                                   int smooth_k, const sage_quantized* out, void* cuda_stream);
+
 /* The attention kernel on a quantized bundle: INT8 QK^T with exact integer
  * accumulation (run on the tcgen05 tensor cores as fp16 x fp16 -> fp32,
  * which is exact for |code| <= 127 and 128 channels), dequantization by

@@ -34,6 +34,8 @@ _SIGNATURES = {
     "sage_quantize": (c_int, [ctypes.POINTER(Bf16Tensor)] * 3 + [c_i64, c_i64, c_i64, c_i64, c_int,
                                                                 ctypes.POINTER(Quantized), c_vp, ctypes.c_size_t,
                                                                 c_vp]),
+    "sage_quantize_noalloc": (c_int, [ctypes.POINTER(Bf16Tensor)] * 3 + [c_i64, c_i64, c_i64, c_i64, c_int,
+                                                                        ctypes.POINTER(Quantized), c_vp]),
     "sage_attention": (c_int, [ctypes.POINTER(Quantized), c_i64, c_i64, c_i64, c_i64, ctypes.c_float, c_vp,
                                c_i64, c_i64, c_i64, c_vp]),
     "sage_attention_simt": (c_int, [ctypes.POINTER(Quantized), c_i64, c_i64, c_i64, c_i64, ctypes.c_float, c_vp,

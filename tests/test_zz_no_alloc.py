@@ -1,0 +1,62 @@
+"""sage_quantize_noalloc: the quantization prologue for callers that cannot
+allocate device memory (code held to a memory budget fixed up front, plug-ins
+handed only the tensors they read and write, hosts whose allocator must not be
+entered from the calling thread). It keeps its scratch in a device array built
+into the library instead of a caller-provided buffer.
+
+Checked through the C ABI against sage_quantize (which takes a caller-owned
+scratch buffer): the codes, scales and key means must be identical, bit for
+bit, as every prologue result is; two different problems run back to back, so
+the second call also shows that what the first left in the shared array does
+not leak into its result. This file sorts last so that a run stopping at the
+first failure has already run every other test."""
+
+import ctypes
+
+import pytest
+import torch
+
+from gpu_util import assert_bundles_equal, bundle_np
+from quantized_attention_fp64_gb300 import _lib
+from quantized_attention_fp64_gb300.api import _bf16_tensor, _stream, alloc_bundle, quantize
+from quantized_attention_fp64_gb300.workloads import custom, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+SAGE_ERR_WORKSPACE = -9
+
+
+def _noalloc(lib, q, k, v, smooth_k):
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    qz = alloc_bundle(B, S, H, q.device)
+    bundle = qz.c_struct()
+    rc = lib.sage_quantize_noalloc(ctypes.byref(_bf16_tensor(q, "NHD")), ctypes.byref(_bf16_tensor(k, "NHD")),
+                                   ctypes.byref(_bf16_tensor(v, "NHD")), B, S, H, 128, int(smooth_k),
+                                   ctypes.byref(bundle), _stream(q.device))
+    assert rc == 0, lib.sage_strerror(rc)
+    return qz
+
+
+def test_noalloc_matches_quantize_twice(sage_lib):
+    lib = _lib.load()
+    problems = [(custom(2, 8, 1024, seed_index=901, k_offset_std=3.0), True),
+                (custom(1, 5, 777, seed_index=902, k_offset_std=1.0), False)]
+    for w, smooth in problems:
+        q, k, v = make_qkv(w, "cuda")
+        got = _noalloc(lib, q, k, v, smooth)
+        ref = quantize(q, k, v, "NHD", smooth)
+        torch.cuda.synchronize()
+        assert_bundles_equal(bundle_np(got), bundle_np(ref))
+
+
+def test_noalloc_rejects_problems_beyond_its_buffer(sage_lib):
+    lib = _lib.load()
+    q = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16, device="cuda")
+    qz = alloc_bundle(1, 64, 2, q.device)
+    bundle = qz.c_struct()
+    t = _bf16_tensor(q, "NHD")
+    # 80 heads x 131072 tokens need about 61 MiB of scratch, over the 32 MiB
+    # built in; the call is refused before anything is launched
+    rc = lib.sage_quantize_noalloc(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), 1, 131072, 80, 128, 1,
+                                   ctypes.byref(bundle), _stream(q.device))
+    assert rc == SAGE_ERR_WORKSPACE
