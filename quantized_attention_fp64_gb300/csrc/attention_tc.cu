@@ -105,6 +105,8 @@ struct Ctx {
 };
 
 // Bounded wait for the phase of `parity` on barrier `bar` to complete.
+// (Inlined everywhere: setmaxnreg gives the roles different register
+// budgets, and one out-of-line copy cannot be allocated for both.)
 __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint32_t bar, uint32_t parity) {
   if (tc::mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
@@ -180,11 +182,11 @@ __device__ __forceinline__ float ex2(float x) {
 // four warps of a warpgroup execute the same instruction). The block is
 // launched with 168 registers per thread (384 x 168 = 64512); the control
 // warpgroup drops to kRegsCtl before its role switch and the softmax
-// warpgroups rise to kRegsSoftmax (128 x 72 + 256 x 216 = 64512). At the end
+// warpgroups rise to kRegsSoftmax (128 x 88 + 256 x 208 = 64512). At the end
 // the softmax warpgroups drop to kRegsCtl too, so the shared teardown runs
 // with one budget in every warp. The changes sit inside the branches so the
 // compiler allocates each branch with its own budget.
-constexpr uint32_t kRegsCtl = 72, kRegsSoftmax = 216;
+constexpr uint32_t kRegsCtl = 88, kRegsSoftmax = 208;
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
@@ -198,6 +200,117 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+
+// S_i = Q_i K^T for one 128-key tile: 8 MMAs of K = 16 over the two
+// 64-channel subtiles of the fp16 Q and K tiles. The empty asm keeps the
+// compiler from hoisting the (loop-invariant) descriptors of every buffer into
+// registers; they are recomputed from the base addresses, a few integer ops.
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t sbase, int i, uint32_t buf) {
+  uint32_t qa = sbase + kOffQ16 + static_cast<uint32_t>(i) * kTile16, ka = sbase + kOffK16 + buf * kTile16;
+  asm volatile("" : "+r"(qa), "+r"(ka));
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t off = static_cast<uint32_t>(ks >> 2) * kSub16 + static_cast<uint32_t>(ks & 3) * 32u;
+    tc::mma_f16_ss(tmem + col_s(i), tc::sw128_desc(qa + off), tc::sw128_desc(ka + off), tc::kIdescM128N128,
+                   ks > 0 ? 1u : 0u);
+  }
+}
+
+// O_i (+)= P_i V for one 128-key tile: 4 MMAs of K = 32, P from TMEM (the
+// first 32 columns of S_i), V^T from shared memory.
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int i, uint32_t vst, bool acc) {
+  uint32_t va = sbase + kOffV + vst * kTile8;
+  asm volatile("" : "+r"(va));
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks)
+    tc::mma_f8_ts(tmem + col_o(i), tmem + col_s(i) + 8u * ks, tc::sw128_desc(va + 32u * ks), tc::kIdescM128N128,
+                  (acc || ks > 0) ? 1u : 0u);
+}
+
+// One 128-key tile of the online softmax for the calling thread's query row
+// (TMEM lane): reads S, updates the running maximum m and row sum l, writes
+// e4m3(p448) into the first 32 columns of S, and rescales O when the maximum
+// grew. kTail masks keys at or past nvalid (the last tile of a ragged S).
+template <bool kTail>
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, const float (&cb)[4], int nvalid, bool first,
+                                             float& m, float& l) {
+  uint32_t sr[4][32];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) tc::tmem_ld32(tS + 32u * b, sr[b]);
+  tc::tmem_wait_ld();
+  if (kTail) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (32 * b + k >= nvalid) sr[b][k] = 0xFF800000u;  // -inf
+  }
+  float mt = -INFINITY;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    float mb = __uint_as_float(sr[b][0]);
+#pragma unroll
+    for (int k = 1; k < 31; k += 2) mb = max3(mb, __uint_as_float(sr[b][k]), __uint_as_float(sr[b][k + 1]));
+    mb = fmaxf(mb, __uint_as_float(sr[b][31]));
+    // the scale is >= 0, so the block maximum of S * c is c times that of S
+    const float xb = mb * cb[b];
+    mt = fmaxf(mt, (kTail && mb == -INFINITY) ? -INFINITY : xb);
+  }
+  const float m_new = fmaxf(m, mt);
+  const bool grew = m_new > m;
+  const float alpha = ex2(m - m_new);  // 0 on the first tile
+  const float neg = kLog2P - m_new;
+  const float2 n2 = make_float2(neg, neg);
+  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const float2 c2 = make_float2(cb[b], cb[b]);
+    uint32_t pw[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(sr[b][4 * k]), __uint_as_float(sr[b][4 * k + 1])),
+                                    c2, n2);
+      const float2 x23 = __ffma2_rn(
+          make_float2(__uint_as_float(sr[b][4 * k + 2]), __uint_as_float(sr[b][4 * k + 3])), c2, n2);
+      float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+      float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+      if (kTail) {
+        const int c0 = 32 * b + 4 * k;
+        if (c0 >= nvalid) p01.x = 0.f;
+        if (c0 + 1 >= nvalid) p01.y = 0.f;
+        if (c0 + 2 >= nvalid) p23.x = 0.f;
+        if (c0 + 3 >= nvalid) p23.y = 0.f;
+      }
+      sa = __fadd2_rn(sa, p01);
+      sb = __fadd2_rn(sb, p23);
+      pw[k] = e4m3x2(p01.y, p01.x) | (e4m3x2(p23.y, p23.x) << 16);
+    }
+    tc::tmem_st8(tS + 8u * b, pw);
+  }
+  l = l * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
+  m = m_new;
+  // O rescale (S is no longer needed, so its registers hold O): PV of the
+  // previous tile has completed, because S of this tile was committed after it.
+  if (!first && __any_sync(0xffffffffu, grew)) {
+    uint32_t o[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tc::tmem_ld32(tO + 32u * c, o[c]);
+    tc::tmem_wait_ld();
+    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        const float2 r = __fmul2_rn(make_float2(__uint_as_float(o[c][k]), __uint_as_float(o[c][k + 1])), a2);
+        o[c][k] = __float_as_uint(r.x);
+        o[c][k + 1] = __float_as_uint(r.y);
+      }
+      tc::tmem_st32(tO + 32u * c, o[c]);
+    }
+  }
+  tc::tmem_wait_st();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -303,25 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA --
     if (lane == 0) {
-      const uint32_t idesc = tc::kIdescM128N128;
       uint32_t k16_cnt = 0, v_cnt = 0, unit_cnt = 0, p_cnt[2] = {0, 0};
       bool ok = true;
-      auto qk = [&](int i, uint32_t buf) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = static_cast<uint32_t>(ks >> 2) * kSub16 + static_cast<uint32_t>(ks & 3) * 32u;
-          const uint64_t a = tc::sw128_desc(sbase + kOffQ16 + i * kTile16 + off);
-          const uint64_t b = tc::sw128_desc(sbase + kOffK16 + buf * kTile16 + off);
-          tc::mma_f16_ss(tmem + col_s(i), a, b, idesc, ks > 0 ? 1u : 0u);
-        }
-      };
-      auto pv = [&](int i, uint32_t vst, bool acc) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t b = tc::sw128_desc(sbase + kOffV + vst * kTile8 + static_cast<uint32_t>(ks) * 32u);
-          tc::mma_f8_ts(tmem + col_o(i), tmem + col_s(i) + 8u * ks, b, idesc, (acc || ks > 0) ? 1u : 0u);
-        }
-      };
       for (int64_t u = blockIdx.x; ok && u < prm.n_units; u += gridDim.x) {
         if (!(ok = wait_bar(cx, cx.bar(kBarQ16Full), unit_cnt & 1u))) break;
         tc::tc_fence_after();
@@ -329,9 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t buf = k16_cnt & 1u;
         if (!(ok = wait_bar(cx, cx.bar(kBarK16Full + buf), (k16_cnt >> 1) & 1u))) break;
         tc::tc_fence_after();
-        qk(0, buf);
+        issue_qk(tmem, sbase, 0, buf);
         tc::mma_commit(cx.bar(kBarSFull + 0));
-        qk(1, buf);
+        issue_qk(tmem, sbase, 1, buf);
         tc::mma_commit(cx.bar(kBarSFull + 1));
         tc::mma_commit(cx.bar(kBarK16Empty + buf));
         ++k16_cnt;
@@ -348,11 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++p_cnt[i];
             if (j == 1 && !(ok = wait_bar(cx, cx.bar(kBarOEmpty + i), (unit_cnt & 1u) ^ 1u))) break;
             tc::tc_fence_after();
-            pv(i, vst, j > 1);  // PV of step j-1
+            issue_pv(tmem, sbase, i, vst, j > 1);  // PV of step j-1
             if (last) {
               tc::mma_commit(cx.bar(kBarOFull + i));
             } else {
-              qk(i, buf);      // QK of step j
+              issue_qk(tmem, sbase, i, buf);  // QK of step j
               tc::mma_commit(cx.bar(kBarSFull + i));
             }
           }
@@ -427,75 +523,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float cq = row_valid ? prm.q_scale[bh * nblk + qrow / kQKBlock] * prm.sm_log2 : 0.0f;
       const float* ks = prm.k_scale + bh * nblk;
       float m = -INFINITY, l = 0.0f;
-      for (int64_t j = 0; j < n_kv; ++j) {
-        float cb[4];
+      float cb[4];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) cb[b] = cq * __ldg(ks + j * 4 + b);
+      for (int b = 0; b < 4; ++b) cb[b] = cq * __ldg(ks + b);
+      for (int64_t j = 0; j < n_kv; ++j) {
         if (!(ok = wait_bar_warp(cx, cx.bar(kBarSFull + i), s_cnt & 1u))) break;
         ++s_cnt;
         tc::tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) tc::tmem_ld32(tS + 32u * b, sr[b]);
-        tc::tmem_wait_ld();
         const int64_t nvalid = prm.S - j * kKeyTile;  // keys of this tile below S
-        const bool tail = nvalid < kKeyTile;
-        if (tail) {
-#pragma unroll
-          for (int b = 0; b < 4; ++b)
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-              if (32 * b + k >= nvalid) sr[b][k] = 0xFF800000u;  // -inf
-        }
-        float mt = -INFINITY;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          float mb = __uint_as_float(sr[b][0]);
-#pragma unroll
-          for (int k = 1; k < 31; k += 2) mb = max3(mb, __uint_as_float(sr[b][k]), __uint_as_float(sr[b][k + 1]));
-          mb = fmaxf(mb, __uint_as_float(sr[b][31]));
-          // the scale is >= 0, so the block maximum of S * c is c times that of S
-          mt = fmaxf(mt, mb == -INFINITY ? -INFINITY : mb * cb[b]);
-        }
-        const float m_new = fmaxf(m, mt);
-        const float alpha = ex2(m - m_new);  // 0 on the first tile
-        if (j > 0 && __any_sync(0xffffffffu, m_new > m)) {
-          // rescale this row's O (PV of the previous step has completed:
-          // S of this step was committed after it)
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tc::tmem_ld32(tO + 32u * c, o);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tc::tmem_st32(tO + 32u * c, o);
-          }
-        }
-        const float neg = kLog2P - m_new;
-        float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          uint32_t pw[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            float p[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float s = __uint_as_float(sr[b][4 * k + e]);
-              p[e] = tail && (32 * b + 4 * k + e >= nvalid) ? 0.0f : ex2(fmaf(s, cb[b], neg));
-            }
-            ls0 += p[0] + p[1];
-            ls1 += p[2] + p[3];
-            pw[k] = e4m3x2(p[1], p[0]) | (e4m3x2(p[3], p[2]) << 16);
-          }
-          tc::tmem_st8(tS + 8u * b, pw);
-        }
-        l = l * alpha + (ls0 + ls1);
-        m = m_new;
-        tc::tmem_wait_st();
+        if (nvalid >= kKeyTile)
+          softmax_tile<false>(tS, tO, cb, kKeyTile, j == 0, m, l);
+        else
+          softmax_tile<true>(tS, tO, cb, static_cast<int>(nvalid), j == 0, m, l);
         tc::tc_fence_before();
         tc::mbar_arrive(cx.bar(kBarPFull + i));
+        if (j + 1 < n_kv) {
+#pragma unroll
+          for (int b = 0; b < 4; ++b) cb[b] = cq * __ldg(ks + (j + 1) * 4 + b);
+        }
       }
       if (!ok) break;
       // epilogue: O = acc * s_v / l (l counts p448), bf16 in the output layout
