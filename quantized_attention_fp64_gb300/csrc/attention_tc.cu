@@ -40,9 +40,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -585,42 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // 3-D byte tensor [d2][d1][d0] with 128 x 128 boxes, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2) {
-  auto fn = get_encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0, d0 * d1};
-  const cuuint32_t box[3] = {128, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-  static int n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  });
-  return n;
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint64_t strides[2] = {d0, d0 * d1};
+  const uint32_t box[3] = {128, 128, 1};
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
@@ -650,7 +617,8 @@ cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t 
   cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(p.n_units < sm_count() ? p.n_units : sm_count());
+  const int sms = sm_count_current();
+  const int grid = static_cast<int>(p.n_units < sms ? p.n_units : sms);
   attention_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -1,6 +1,7 @@
 // Shared definitions for the CUDA side of the library (kernels and C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -43,6 +44,13 @@ struct Out {
   uint16_t* p;
   int64_t sb, ss, sh;
 };
+
+// TMA tensor map over `rank` dimensions (dims[0] contiguous); strides_bytes
+// holds rank-1 byte strides of dims 1..rank-1. Returns false on failure.
+bool make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+               const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
+int sm_count_current();        // SMs of the current device (cached)
+size_t l2_bytes_current();     // L2 bytes of the current device (cached)
 
 // Launchers implemented by the kernel translation units. Each enqueues on
 // `stream` and returns the launch status (cudaGetLastError).
