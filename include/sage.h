@@ -108,7 +108,13 @@ typedef struct sage_bf16_tensor {
  *   vt_codes         : e4m3fn [B][H][128][S_pad]   (V transposed; cols S..S_pad-1 are 0)
  *   q_scale, k_scale : float  [B][H][S_pad/32]     (blocks past ceil(S/32) are 0)
  *   v_scale          : float  [B][H][128]
- *   k_mean           : float  [B][H][128]          (0 when smooth_k is off) */
+ *   k_mean           : float  [B][H][128]          (0 when smooth_k is off)
+ *   q16, k16         : fp16   [B][H][S_pad][128]   the same Q and K codes as fp16
+ *                      values (exact: |code| <= 127). sm_103a has no integer
+ *                      tensor-core MMA, so the attention kernel multiplies the
+ *                      codes on the fp16 tensor cores; writing them once here
+ *                      saves every CTA of the attention kernel from re-widening
+ *                      each key tile. */
 typedef struct sage_quantized {
   int8_t* q_codes_dev;
   int8_t* k_codes_dev;
@@ -117,6 +123,8 @@ typedef struct sage_quantized {
   float* k_scale_dev;
   float* v_scale_dev;
   float* k_mean_dev;
+  uint16_t* q16_dev;
+  uint16_t* k16_dev;
 } sage_quantized;
 
 /* ----------------------------------------------------------- size queries -- */

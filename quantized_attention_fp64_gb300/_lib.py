@@ -24,7 +24,8 @@ class Bf16Tensor(ctypes.Structure):
 class Quantized(ctypes.Structure):
     """sage_quantized"""
     _fields_ = [("q_codes_dev", c_vp), ("k_codes_dev", c_vp), ("vt_codes_dev", c_vp), ("q_scale_dev", c_vp),
-                ("k_scale_dev", c_vp), ("v_scale_dev", c_vp), ("k_mean_dev", c_vp)]
+                ("k_scale_dev", c_vp), ("v_scale_dev", c_vp), ("k_mean_dev", c_vp), ("q16_dev", c_vp),
+                ("k16_dev", c_vp)]
 
 
 _SIGNATURES = {

@@ -80,13 +80,16 @@ class QuantizedQKV:
     k_scale: torch.Tensor   # float32 [B, H, S_pad/32]
     v_scale: torch.Tensor   # float32 [B, H, 128]
     k_mean: torch.Tensor    # float32 [B, H, 128]
+    q16: torch.Tensor       # float16 [B, H, S_pad, 128], the Q codes as fp16 values
+    k16: torch.Tensor       # float16 [B, H, S_pad, 128], the K codes as fp16 values
     B: int
     S: int
     H: int
 
     def c_struct(self) -> _lib.Quantized:
         return _lib.Quantized(*(t.data_ptr() for t in (self.q_codes, self.k_codes, self.vt_codes, self.q_scale,
-                                                       self.k_scale, self.v_scale, self.k_mean)))
+                                                       self.k_scale, self.v_scale, self.k_mean, self.q16,
+                                                       self.k16)))
 
 
 def alloc_bundle(B: int, S: int, H: int, device) -> QuantizedQKV:
@@ -116,6 +119,8 @@ def alloc_bundle(B: int, S: int, H: int, device) -> QuantizedQKV:
         k_scale=view(c.k_scale_dev, torch.float32, (B, H, s_pad // 32)),
         v_scale=view(c.v_scale_dev, torch.float32, (B, H, 128)),
         k_mean=view(c.k_mean_dev, torch.float32, (B, H, 128)),
+        q16=view(c.q16_dev, torch.float16, (B, H, s_pad, 128)),
+        k16=view(c.k16_dev, torch.float16, (B, H, s_pad, 128)),
         B=B, S=S, H=H)
 
 

@@ -67,20 +67,22 @@ bool stride_ok(int64_t s) { return s % 8 == 0; }
 
 size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 
+constexpr int kBundleArrays = 9;
+
 struct BundleLayout {
-  size_t off[7];
+  size_t off[kBundleArrays];
   size_t total;
 };
 
 BundleLayout bundle_layout(int64_t B, int64_t S, int64_t H) {
   const size_t bh = static_cast<size_t>(B * H);
   const size_t sp = static_cast<size_t>(padded_len(S));
-  const size_t sizes[7] = {bh * sp * kHeadDim, bh * sp * kHeadDim, bh * sp * kHeadDim,
-                           bh * (sp / kQKBlock) * 4, bh * (sp / kQKBlock) * 4, bh * kHeadDim * 4,
-                           bh * kHeadDim * 4};
+  const size_t sizes[kBundleArrays] = {bh * sp * kHeadDim,         bh * sp * kHeadDim,         bh * sp * kHeadDim,
+                                       bh * (sp / kQKBlock) * 4,   bh * (sp / kQKBlock) * 4,   bh * kHeadDim * 4,
+                                       bh * kHeadDim * 4,          bh * sp * kHeadDim * 2,     bh * sp * kHeadDim * 2};
   BundleLayout l;
   size_t o = 0;
-  for (int i = 0; i < 7; ++i) {
+  for (int i = 0; i < kBundleArrays; ++i) {
     l.off[i] = o;
     o += round256(sizes[i]);
   }
@@ -98,14 +100,17 @@ Bundle carve(void* base, const BundleLayout& l) {
   b.k_scale = reinterpret_cast<float*>(c + l.off[4]);
   b.v_scale = reinterpret_cast<float*>(c + l.off[5]);
   b.k_mean = reinterpret_cast<float*>(c + l.off[6]);
+  b.q16 = reinterpret_cast<uint16_t*>(c + l.off[7]);
+  b.k16 = reinterpret_cast<uint16_t*>(c + l.off[8]);
   return b;
 }
 
 int check_bundle(const sage_quantized* in, bool need_mean) {
   if (in == nullptr) return SAGE_ERR_NULLPTR;
-  const void* ptrs[7] = {in->q_codes_dev, in->k_codes_dev, in->vt_codes_dev, in->q_scale_dev,
-                         in->k_scale_dev, in->v_scale_dev, in->k_mean_dev};
-  for (int i = 0; i < 7; ++i) {
+  const void* ptrs[kBundleArrays] = {in->q_codes_dev, in->k_codes_dev, in->vt_codes_dev,
+                                     in->q_scale_dev, in->k_scale_dev,  in->v_scale_dev,
+                                     in->k_mean_dev,  in->q16_dev,      in->k16_dev};
+  for (int i = 0; i < kBundleArrays; ++i) {
     if (i == 6 && !need_mean) continue;
     if (ptrs[i] == nullptr) return SAGE_ERR_NULLPTR;
     if (!aligned16(ptrs[i])) return SAGE_ERR_ALIGN;
@@ -122,6 +127,8 @@ Bundle to_bundle(const sage_quantized* in) {
   b.k_scale = in->k_scale_dev;
   b.v_scale = in->v_scale_dev;
   b.k_mean = in->k_mean_dev;
+  b.q16 = in->q16_dev;
+  b.k16 = in->k16_dev;
   return b;
 }
 
@@ -186,6 +193,8 @@ int sage_bundle_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes, 
     bundle->k_scale_dev = b.k_scale;
     bundle->v_scale_dev = b.v_scale;
     bundle->k_mean_dev = b.k_mean;
+    bundle->q16_dev = b.q16;
+    bundle->k16_dev = b.k16;
   }
   return SAGE_OK;
 }

@@ -37,6 +37,8 @@ struct Bundle {
   float* k_scale;
   float* v_scale;
   float* k_mean;
+  uint16_t* q16;  // fp16 copies of the codes, [B][H][S_pad][128]
+  uint16_t* k16;
 };
 
 // BF16 output: element (b, s, h, d) at p[b*sb + s*ss + h*sh + d].

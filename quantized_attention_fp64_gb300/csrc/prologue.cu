@@ -38,6 +38,8 @@
 // exact division decides. For e4m3, rounding is monotone, so when q scaled by
 // (1 - 2^-21) and by (1 + 2^-21) round to the same code, fl(v/s) (within
 // 2^-22 relative of q) does too; otherwise the exact division decides.
+#include <cuda_fp16.h>
+
 #include <cfloat>
 
 #include "common.cuh"
@@ -97,11 +99,24 @@ __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint3
   return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
+// Four int8 codes (one word) as four fp16 values, exactly: the fp16 bit
+// pattern 0x6400 | (c ^ 0x80) is 1024 + c + 128, and subtracting 1152 leaves c.
+__device__ __forceinline__ uint2 codes_to_f16x4(uint32_t w) {
+  const uint32_t x = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(x, 0x64646464u, 0x5140);
+  const uint32_t b = __byte_perm(x, 0x64646464u, 0x7362);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&ha), *reinterpret_cast<uint32_t*>(&hb));
+}
+
 // INT8 codes and scale of one 32-token block held by a warp (4 channels per
-// lane). Writes rows s0..s0+31 of codes_bh ([S_pad][128]); returns the scale.
+// lane). Writes rows s0..s0+31 of codes_bh ([S_pad][128]) and the same codes
+// as fp16 values to f16_bh ([S_pad][128]); returns the scale.
 template <bool kSub>
 __device__ __forceinline__ float quantize_int8_block(const uint2 (&w)[32], const float (&mu)[4], int nvalid,
-                                                     int8_t* codes_bh, int64_t s0, int lane) {
+                                                     int8_t* codes_bh, uint16_t* f16_bh, int64_t s0, int lane) {
   float a = 0.0f;
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
@@ -118,6 +133,7 @@ __device__ __forceinline__ float quantize_int8_block(const uint2 (&w)[32], const
   const bool fast = s >= FLT_MIN;
   const float r = fast ? __frcp_rn(s) : 0.0f;
   uint32_t* out = reinterpret_cast<uint32_t*>(codes_bh + s0 * kHeadDim) + lane;
+  uint2* out16 = reinterpret_cast<uint2*>(f16_bh + s0 * kHeadDim) + lane;
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
     uint32_t word = 0u;
@@ -131,6 +147,7 @@ __device__ __forceinline__ float quantize_int8_block(const uint2 (&w)[32], const
       word = pack_low_bytes(bits[0], bits[1], bits[2], bits[3]);
     }
     out[t * (kHeadDim / 4)] = word;
+    out16[t * (kHeadDim / 4)] = codes_to_f16x4(word);
   }
   return s;
 }
@@ -214,7 +231,8 @@ __global__ void __launch_bounds__(kGroup) prologue_stats_kernel(Bf16In q, Bf16In
   if (s0 < S_pad) {
     const float zero[4] = {0.f, 0.f, 0.f, 0.f};
     load_chunk(w, q, b, h, s0, nvalid, lane);
-    const float s = quantize_int8_block<false>(w, zero, nvalid, out.q_codes + bh * S_pad * kHeadDim, s0, lane);
+    const float s = quantize_int8_block<false>(w, zero, nvalid, out.q_codes + bh * S_pad * kHeadDim,
+                                               out.q16 + bh * S_pad * kHeadDim, s0, lane);
     if (lane == 0) out.q_scale[bh * (S_pad / kQKBlock) + s0 / kQKBlock] = s;
   }
   // Exact fp64 key sums of the chunk.
@@ -310,8 +328,9 @@ __global__ void __launch_bounds__(kGroup) prologue_quant_kernel(Bf16In k, Bf16In
   for (int c = 0; c < 4; ++c) mu[c] = smooth_k ? out.k_mean[bh * kHeadDim + 4 * lane + c] : 0.0f;
   load_chunk(w, k, b, h, s0, nvalid, lane);
   int8_t* kc = out.k_codes + bh * S_pad * kHeadDim;
-  const float sk = smooth_k ? quantize_int8_block<true>(w, mu, nvalid, kc, s0, lane)
-                            : quantize_int8_block<false>(w, mu, nvalid, kc, s0, lane);
+  uint16_t* k16 = out.k16 + bh * S_pad * kHeadDim;
+  const float sk = smooth_k ? quantize_int8_block<true>(w, mu, nvalid, kc, k16, s0, lane)
+                            : quantize_int8_block<false>(w, mu, nvalid, kc, k16, s0, lane);
   if (lane == 0) out.k_scale[bh * (S_pad / kQKBlock) + s0 / kQKBlock] = sk;
 
   // V codes, transposed to [channel][token].

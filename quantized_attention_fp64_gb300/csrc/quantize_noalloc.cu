@@ -95,8 +95,8 @@ extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_
   int rc;
   if ((rc = check_in(q)) != SAGE_OK || (rc = check_in(k)) != SAGE_OK || (rc = check_in(v)) != SAGE_OK) return rc;
   if (out == nullptr) return SAGE_ERR_NULLPTR;
-  const void* ptrs[7] = {out->q_codes_dev, out->k_codes_dev, out->vt_codes_dev, out->q_scale_dev,
-                         out->k_scale_dev, out->v_scale_dev, out->k_mean_dev};
+  const void* ptrs[9] = {out->q_codes_dev, out->k_codes_dev, out->vt_codes_dev, out->q_scale_dev, out->k_scale_dev,
+                         out->v_scale_dev, out->k_mean_dev,  out->q16_dev,      out->k16_dev};
   for (const void* p : ptrs) {
     if (p == nullptr) return SAGE_ERR_NULLPTR;
     if (!aligned16(p)) return SAGE_ERR_ALIGN;
@@ -110,8 +110,8 @@ extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_
   const Bf16In qi{static_cast<const uint16_t*>(q->ptr_dev), q->stride_b, q->stride_s, q->stride_h};
   const Bf16In ki{static_cast<const uint16_t*>(k->ptr_dev), k->stride_b, k->stride_s, k->stride_h};
   const Bf16In vi{static_cast<const uint16_t*>(v->ptr_dev), v->stride_b, v->stride_s, v->stride_h};
-  const Bundle bo{out->q_codes_dev, out->k_codes_dev, out->vt_codes_dev, out->q_scale_dev,
-                  out->k_scale_dev, out->v_scale_dev, out->k_mean_dev};
+  const Bundle bo{out->q_codes_dev, out->k_codes_dev, out->vt_codes_dev, out->q_scale_dev, out->k_scale_dev,
+                  out->v_scale_dev, out->k_mean_dev,  out->q16_dev,      out->k16_dev};
   const cudaError_t e =
       launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, bo, scratch, static_cast<cudaStream_t>(cuda_stream));
   return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;

@@ -16,6 +16,10 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 
 
 def bundle_np(qz):
+    """The bundle as numpy arrays; also checks that the fp16 copies of the Q
+    and K codes equal the int8 codes exactly."""
+    assert torch.equal(qz.q16.float(), qz.q_codes.float()), "q16 differs from the int8 Q codes"
+    assert torch.equal(qz.k16.float(), qz.k_codes.float()), "k16 differs from the int8 K codes"
     return dict(q_codes=qz.q_codes.cpu().numpy(), k_codes=qz.k_codes.cpu().numpy(),
                 vt_codes=qz.vt_codes.cpu().numpy(), q_scale=qz.q_scale.cpu().numpy(),
                 k_scale=qz.k_scale.cpu().numpy(), v_scale=qz.v_scale.cpu().numpy(),

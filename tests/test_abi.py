@@ -51,7 +51,7 @@ def test_size_queries(lib):
     n = ctypes.c_size_t(0)
     assert lib.sage_bundle_size(B, S, H, 128, ctypes.byref(n), None, None) == OK
     # codes: 3 x B*H*S_pad*128 bytes; scales and means are small
-    assert n.value >= 3 * B * H * S * 128
+    assert n.value >= 7 * B * H * S * 128   # int8/e4m3 codes (3) + fp16 Q/K copies (4)
     assert ws == n.value + sc
     # scratch: fp64 + fp32 per (head, 256-token group, channel), 256-aligned
     assert sc == 28 * 64 * 128 * 8 + 28 * 64 * 128 * 4
@@ -66,9 +66,10 @@ def test_bundle_carve_alignment(lib):
     n = ctypes.c_size_t(0)
     c = _lib.Quantized()
     assert lib.sage_bundle_size(2, 1000, 3, 128, ctypes.byref(n), ctypes.c_void_p(0x100000), ctypes.byref(c)) == OK
-    ptrs = [c.q_codes_dev, c.k_codes_dev, c.vt_codes_dev, c.q_scale_dev, c.k_scale_dev, c.v_scale_dev, c.k_mean_dev]
+    ptrs = [c.q_codes_dev, c.k_codes_dev, c.vt_codes_dev, c.q_scale_dev, c.k_scale_dev, c.v_scale_dev, c.k_mean_dev,
+            c.q16_dev, c.k16_dev]
     assert ptrs[0] == 0x100000 and all(p % 256 == 0 for p in ptrs)
-    assert ptrs == sorted(ptrs) and ptrs[-1] + 2 * 3 * 128 * 4 <= 0x100000 + n.value
+    assert ptrs == sorted(ptrs) and ptrs[-1] + 2 * 3 * 1024 * 128 * 2 <= 0x100000 + n.value
     assert lib.sage_bundle_size(2, 1000, 3, 128, ctypes.byref(n), ctypes.c_void_p(0x100010), ctypes.byref(c)) == ALIGN
 
 
@@ -113,14 +114,16 @@ def test_quantize_and_attention_rejections(lib):
     t = _lib.Bf16Tensor(0x10000, 65536, 256, 128)
     bad = _lib.Bf16Tensor(0x10002, 65536, 256, 128)
     nul = _lib.Bf16Tensor(0, 65536, 256, 128)
-    qz = _lib.Quantized(0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000)
+    qz = _lib.Quantized(0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000, 0x800000,
+                        0x900000)
     r = ctypes.byref
     assert lib.sage_quantize(r(t), r(t), r(t), 1, 256, 2, 64, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == HEAD_DIM
     assert lib.sage_quantize(r(bad), r(t), r(t), 1, 256, 2, 128, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == ALIGN
     assert lib.sage_quantize(r(t), r(nul), r(t), 1, 256, 2, 128, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == NULLPTR
     assert lib.sage_quantize(r(t), r(t), r(t), 1, 256, 2, 128, 1, r(qz), ctypes.c_void_p(0x800000), 16, None) == WORKSPACE
     assert lib.sage_quantize(r(t), r(t), r(t), 1, 256, 2, 128, 1, r(qz), None, 1 << 30, None) == NULLPTR
-    qz_bad = _lib.Quantized(0x100000, 0x200004, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000)
+    qz_bad = _lib.Quantized(0x100000, 0x200004, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000, 0x800000,
+                            0x900000)
     out = ctypes.c_void_p(0x900000)
     for fn in ("sage_attention", "sage_attention_simt"):
         f = getattr(lib, fn)
