@@ -138,8 +138,9 @@ typedef struct sage_quantized {
 SAGE_API int sage_bundle_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes,
                      void* base_dev, sage_quantized* bundle);
 
-/* Scratch bytes sage_quantize needs (per-256-token partial key sums in fp64
- * and partial V maxima). Errors: as sage_bundle_size. */
+/* Scratch bytes sage_quantize needs (a work counter and per-head flags,
+ * per-256-token partial key sums in fp64 and partial V maxima).
+ * Errors: as sage_bundle_size. */
 SAGE_API int sage_quantize_scratch_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes);
 
 /* Workspace bytes sage_sageattn needs: one bundle plus the quantize scratch. */
@@ -152,8 +153,9 @@ SAGE_API int sage_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, siz
  * q, k, v: BF16 tensors of shape (B, S, H, 128) with the given strides.
  * scratch_dev: at least sage_quantize_scratch_size bytes, 256-byte aligned;
  * its contents on entry do not matter and are clobbered.
- * Three kernels are enqueued: statistics + Q codes, per-head finalisation
- * (key mean, V scales), then K and V codes.
+ * Enqueued: a clear of the scratch header (work counter, per-head flags) and
+ * one persistent kernel that computes the statistics and Q codes, finishes
+ * each head (key mean, V scales), then writes the K and V codes.
  * Errors: NULLPTR, SHAPE, HEAD_DIM, ALIGN, WORKSPACE, TOO_LARGE, ARCH, CUDA. */
 SAGE_API int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k, const sage_bf16_tensor* v,
                   int64_t B, int64_t S, int64_t H, int64_t D, int smooth_k,
@@ -175,9 +177,10 @@ SAGE_API int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k,
  * rejected with SAGE_ERR_WORKSPACE and nothing is launched.
  * The first call on each device looks up the array's device address with
  * cudaGetSymbolAddress; make that first call before any stream capture.
- * All calls share the array and it keeps the last call's contents (nothing in
- * it needs to start at zero); calls whose work overlaps on the GPU race on it,
- * so order them on one stream. Allocates nothing; results are identical to
+ * All calls share the array and it keeps the last call's contents; each call
+ * clears the part that must start at zero (a work counter and per-head flags)
+ * before its kernel runs. Calls whose work overlaps on the GPU race on the
+ * array, so order them on one stream. Allocates nothing; results are identical to
  * sage_quantize's.
  * Errors: NULLPTR, SHAPE, HEAD_DIM, ALIGN, WORKSPACE, TOO_LARGE, ARCH, CUDA. */
 SAGE_API int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_tensor* k,

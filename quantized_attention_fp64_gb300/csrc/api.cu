@@ -169,6 +169,13 @@ int attention_common(const sage_quantized* in, int64_t B, int64_t S, int64_t H, 
 }
 
 }  // namespace
+
+int* device_error_ptr() {
+  int dev = 0;
+  if (check_device(&dev) != SAGE_OK) return nullptr;
+  return g_err_ptr[dev];
+}
+
 }  // namespace sage
 
 using namespace sage;
@@ -232,8 +239,8 @@ int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k, const sa
   const Bf16In qi{static_cast<const uint16_t*>(q->ptr_dev), q->stride_b, q->stride_s, q->stride_h};
   const Bf16In ki{static_cast<const uint16_t*>(k->ptr_dev), k->stride_b, k->stride_s, k->stride_h};
   const Bf16In vi{static_cast<const uint16_t*>(v->ptr_dev), v->stride_b, v->stride_s, v->stride_h};
-  return cuda_status(launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, to_bundle(out), scratch_dev,
-                                     static_cast<cudaStream_t>(cuda_stream)));
+  return cuda_status(launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, to_bundle(out), scratch_dev, true,
+                                     g_err_ptr[dev], static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int sage_attention(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
@@ -298,8 +305,11 @@ int sage_sageattn(const void* q_dev, const void* k_dev, const void* v_dev, const
   const Bf16In qi{static_cast<const uint16_t*>(q_dev), qt.stride_b, qt.stride_s, qt.stride_h};
   const Bf16In ki{static_cast<const uint16_t*>(k_dev), kt.stride_b, kt.stride_s, kt.stride_h};
   const Bf16In vi{static_cast<const uint16_t*>(v_dev), vt.stride_b, vt.stride_s, vt.stride_h};
+  // the int8 Q/K codes are not read by the attention kernel, so this path
+  // keeps only their fp16 copies
   if ((rc = cuda_status(launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, bundle,
-                                        static_cast<char*>(workspace_dev) + bl.total, stream))) != SAGE_OK)
+                                        static_cast<char*>(workspace_dev) + bl.total, false, g_err_ptr[dev],
+                                        stream))) != SAGE_OK)
     return rc;
   const Out o{static_cast<uint16_t*>(out_dev), out_strides[0], out_strides[ax_s], out_strides[ax_h]};
   return cuda_status(launch_attention_tc(bundle, B, S, H, scale, o, g_err_ptr[dev], stream));

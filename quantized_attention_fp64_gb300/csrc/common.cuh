@@ -56,9 +56,14 @@ size_t l2_bytes_current();     // L2 bytes of the current device (cached)
 
 // Launchers implemented by the kernel translation units. Each enqueues on
 // `stream` and returns the launch status (cudaGetLastError).
+// write_int8: also store the int8 Q/K codes (the fp16 copies, V codes and
+// all scales are always written). dev_err: the device error word.
 cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, int64_t B, int64_t S,
-                            int64_t H, bool smooth_k, const Bundle& out, void* scratch,
-                            cudaStream_t stream);
+                            int64_t H, bool smooth_k, const Bundle& out, void* scratch, bool write_int8,
+                            int* dev_err, cudaStream_t stream);
+// Device address of the current device's error word (set up on first use),
+// or nullptr if the runtime call fails.
+int* device_error_ptr();
 size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H);
 
 cudaError_t launch_attention_simt(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale,

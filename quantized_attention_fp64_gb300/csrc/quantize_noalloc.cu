@@ -18,8 +18,9 @@
 // capture begins.
 //
 // All calls share the one array, and it keeps whatever the last call left.
-// Nothing in it has to start at zero: every slot the finalize kernel reads
-// is written earlier in the same call by the statistics kernel. Calls whose
+// The prologue clears the part that must start at zero (its work counter and
+// per-head flags) at the start of every call; every other slot it reads is
+// written earlier in the same call. Calls whose
 // work overlaps on the GPU (on different streams, or from different host
 // threads without ordering) race on the array; order them on one stream.
 #include <cuda_runtime.h>
@@ -112,7 +113,9 @@ extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_
   const Bf16In vi{static_cast<const uint16_t*>(v->ptr_dev), v->stride_b, v->stride_s, v->stride_h};
   const Bundle bo{out->q_codes_dev, out->k_codes_dev, out->vt_codes_dev, out->q_scale_dev, out->k_scale_dev,
                   out->v_scale_dev, out->k_mean_dev,  out->q16_dev,      out->k16_dev};
-  const cudaError_t e =
-      launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, bo, scratch, static_cast<cudaStream_t>(cuda_stream));
+  int* dev_err = device_error_ptr();
+  if (dev_err == nullptr) return SAGE_ERR_CUDA;
+  const cudaError_t e = launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, bo, scratch, true, dev_err,
+                                        static_cast<cudaStream_t>(cuda_stream));
   return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }

@@ -63,6 +63,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// 4-D tiled load into shared memory, completing `bytes` on mbarrier `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
+                                            int32_t c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tensor-core operand fetches).
 __device__ __forceinline__ void fence_proxy_async_smem() {
