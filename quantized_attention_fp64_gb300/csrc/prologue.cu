@@ -56,7 +56,8 @@ namespace sage {
 namespace {
 
 constexpr int kWarps = kGroup / 32;            // 8 compute warps
-constexpr int kThreads = kGroup + 32;          // + the producer warp
+constexpr int kTeams = 2;                      // compute teams of kWarps warps
+constexpr int kThreads = kTeams * kGroup + 32; // + the producer warp
 constexpr int kStages = 3;
 constexpr uint32_t kTileBytes = kGroup * kHeadDim * 2;  // one bf16 tile: 256 tokens x 128 channels
 constexpr float kMagic = 12582912.0f;          // 1.5 * 2^23: q + kMagic = rint_even(q) + kMagic for |q| < 2^22
@@ -220,28 +221,37 @@ __device__ __noinline__ double fp64_chunk_sum(const uint8_t* rows, int nvalid, i
 }
 
 // Exact fp64 chunk sums of the lane's 4 channels over the warp's rows (see
-// the file comment for why the float-pair path is bit-identical).
+// the file comment for why the float-pair path is bit-identical). Even and
+// odd tokens run in two float-pair chains for instruction-level parallelism;
+// joining them adds one more error term to lo, inside the same bound.
 __device__ __forceinline__ void chunk_sums(const uint8_t* rows, int nvalid, int lane, double (&out)[4]) {
-  float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f}, am[4] = {0.f, 0.f, 0.f, 0.f};
-  uint32_t umin = 0xFFFFFFFFu;  // (|bits| - 1) of the smallest nonzero magnitude; zeros wrap to all-ones
-#pragma unroll 8
-  for (int t = 0; t < 32; ++t) {
-    if (t < nvalid) {
-      const uint2 w = tok(rows, t, lane);
+  float hi[2][4], lo[2][4], am[2][4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float x = chan(w, c);
-        const float s = __fadd_rn(hi[c], x);
-        const float bb = __fsub_rn(s, hi[c]);
-        const float err = __fadd_rn(__fsub_rn(hi[c], __fsub_rn(s, bb)), __fsub_rn(x, bb));
-        hi[c] = s;
-        lo[c] = __fadd_rn(lo[c], err);
-        am[c] = __fadd_rn(am[c], fabsf(x));
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) hi[k][c] = lo[k][c] = am[k][c] = 0.0f;
+  uint32_t umin = 0xFFFFFFFFu;  // (|bits| - 1) of the smallest nonzero magnitude; zeros wrap to all-ones
+#pragma unroll 4
+  for (int t = 0; t < 32; t += 2) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (t + k < nvalid) {
+        const uint2 w = tok(rows, t + k, lane);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float x = chan(w, c);
+          const float s = __fadd_rn(hi[k][c], x);
+          const float bb = __fsub_rn(s, hi[k][c]);
+          const float err = __fadd_rn(__fsub_rn(hi[k][c], __fsub_rn(s, bb)), __fsub_rn(x, bb));
+          hi[k][c] = s;
+          lo[k][c] = __fadd_rn(lo[k][c], err);
+          am[k][c] = __fadd_rn(am[k][c], fabsf(x));
+        }
+        umin = min(umin, (w.x & 0x7FFFu) - 1u);
+        umin = min(umin, ((w.x >> 16) & 0x7FFFu) - 1u);
+        umin = min(umin, (w.y & 0x7FFFu) - 1u);
+        umin = min(umin, ((w.y >> 16) & 0x7FFFu) - 1u);
       }
-      umin = min(umin, (w.x & 0x7FFFu) - 1u);
-      umin = min(umin, ((w.x >> 16) & 0x7FFFu) - 1u);
-      umin = min(umin, (w.y & 0x7FFFu) - 1u);
-      umin = min(umin, ((w.y >> 16) & 0x7FFFu) - 1u);
     }
   }
   int ef = static_cast<int>(((umin + 1u) >> 7) & 0xFFu);
@@ -249,8 +259,14 @@ __device__ __forceinline__ void chunk_sums(const uint8_t* rows, int nvalid, int 
   const int lsb = ef - 127 - 7;         // L: exponent of the smallest last-bit weight
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const int ea = static_cast<int>((__float_as_uint(am[c]) >> 23) & 0xFFu) - 127;
-    out[c] = ea - lsb <= 41 ? __dadd_rn(static_cast<double>(hi[c]), static_cast<double>(lo[c]))
+    // join the chains: TwoSum of the high parts, the error joins lo
+    const float s = __fadd_rn(hi[0][c], hi[1][c]);
+    const float bb = __fsub_rn(s, hi[0][c]);
+    const float err = __fadd_rn(__fsub_rn(hi[0][c], __fsub_rn(s, bb)), __fsub_rn(hi[1][c], bb));
+    const float l = __fadd_rn(__fadd_rn(lo[0][c], lo[1][c]), err);
+    const float a = __fadd_rn(am[0][c], am[1][c]);
+    const int ea = static_cast<int>((__float_as_uint(a) >> 23) & 0xFFu) - 127;
+    out[c] = ea - lsb <= 40 ? __dadd_rn(static_cast<double>(s), static_cast<double>(l))
                             : fp64_chunk_sum(rows, nvalid, lane, c);
   }
 }
@@ -302,7 +318,8 @@ __device__ __forceinline__ double tree_sum(const double* p, int64_t n) {
   return carry;
 }
 
-__device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kGroup) : "memory"); }
+// Barrier of one compute team (named barrier 1 + team, 256 threads).
+__device__ __forceinline__ void team_bar(int team) { asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "n"(kGroup) : "memory"); }
 
 struct Ctx {
   uint32_t bar0;
@@ -365,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float fin_vmax[kHeadDim];
   __shared__ double fin_right[kHeadDim];
   __shared__ int last_flag;  // stats items: this CTA finished the head
-  __shared__ int ready_ok;   // codes items: the head's statistics are published
+  __shared__ int ready_ok[kTeams];  // codes items: the head's statistics are published
   const uint32_t sbase = tc::smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t* meta_item = reinterpret_cast<int64_t*>(smem + kOffMeta);             // [kStages]
@@ -378,13 +395,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     *cx.abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(cx.full(s), 1);
-      tc::mbar_init(cx.empty(s), kGroup);
+      tc::mbar_init(cx.empty(s), kTeams * kGroup);  // both teams release every stage
     }
     tc::fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kWarps) {
+  if (warp == kTeams * kWarps) {
     // -------------------------------------------------------------- producer --
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
@@ -447,66 +464,80 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // --------------------------------------------------------------- compute --
+  // Two teams of 8 warps work on different tiles of the same item: team 0 on
+  // the first tile (Q of a stats item, K of a codes item), team 1 on the rest
+  // (K sums and V maxima of a stats item, V codes of a codes item). Both
+  // teams wait on every stage in ring order, so a parity wait never meets a
+  // barrier two phases behind; a team releases the stages it does not use as
+  // soon as they are full, and a stage is refilled once both have released it.
+  const int team = warp / kWarps, tw = warp % kWarps, tt = threadIdx.x % kGroup;
   const int64_t S = prm.S, S_pad = prm.S_pad, G = prm.G;
   uint32_t cnt = 0;
+  // wait for ring position c to be full, then release it unused
+  auto pass = [&](uint32_t c) -> bool {
+    if (!wait_bar(cx, cx.full(c % kStages), (c / kStages) & 1u)) return false;
+    tc::mbar_arrive(cx.empty(c % kStages));
+    return true;
+  };
   while (true) {
     const uint32_t st = cnt % kStages;
     if (!wait_bar(cx, cx.full(st), (cnt / kStages) & 1u)) break;
     const int64_t item = meta_item[st];
-    const int tensor = meta_tensor[st];
-    if (tensor == kEnd) break;
+    if (meta_tensor[st] == kEnd) break;
     const Item it = decode_item(item, prm.NH, G, prm.lag);
+    const uint32_t n_stages = it.phase == 0 ? (prm.smooth_k ? 3u : 2u) : 2u;
     const int64_t bh = it.bh;
-    const int64_t s0 = it.g * kGroup + warp * 32;
+    const int64_t s0 = it.g * kGroup + tw * 32;
     const int nvalid = valid_in_chunk(S, s0);
     const bool in_pad = s0 < S_pad;  // rows past S_pad do not exist in the outputs
-    const uint8_t* tile = smem + st * kTileBytes;
+    if (team == 1) tc::mbar_arrive(cx.empty(st));  // the first tile is team 0's
+    const uint32_t mine = cnt + static_cast<uint32_t>(team);  // this team's first ring position
+    const uint8_t* rows = smem + (mine % kStages) * kTileBytes + tw * 32 * 256;
+    bool ok = true;
 
-    if (it.phase == 0) {
-      // ----------------------------------------------------------- stats --
-      // Q tile
+    if (team == 0 && it.phase == 0) {
+      // Q codes and scale
       if (in_pad) {
         const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-        const float s = quantize_int8_block(tile + warp * 32 * 256, zero, nvalid,
+        const float s = quantize_int8_block(rows, zero, nvalid,
                                             prm.write_int8 ? prm.out.q_codes + bh * S_pad * kHeadDim : nullptr,
                                             prm.out.q16 + bh * S_pad * kHeadDim, s0, lane);
         if (lane == 0) prm.out.q_scale[bh * (S_pad / kQKBlock) + s0 / kQKBlock] = s;
       }
       tc::mbar_arrive(cx.empty(st));
-      ++cnt;
+      for (uint32_t c = 1; c < n_stages && ok; ++c) ok = pass(cnt + c);
+      if (!ok) break;
+    } else if (team == 1 && it.phase == 0) {
       // K tile: exact fp64 chunk sums
+      uint32_t c2 = mine;
+      if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
       if (prm.smooth_k) {
-        const uint32_t sk = cnt % kStages;
-        if (!wait_bar(cx, cx.full(sk), (cnt / kStages) & 1u)) break;
         double sums[4];
-        chunk_sums(smem + sk * kTileBytes + warp * 32 * 256, nvalid, lane, sums);
-        tc::mbar_arrive(cx.empty(sk));
-        ++cnt;
+        chunk_sums(rows, nvalid, lane, sums);
+        tc::mbar_arrive(cx.empty(c2 % kStages));
+        ++c2;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ks[warp][4 * lane + c] = sums[c];
+        for (int c = 0; c < 4; ++c) ks[tw][4 * lane + c] = sums[c];
       }
       // V tile: max |v| per channel (bf16 magnitudes compare as integers)
-      {
-        const uint32_t sv = cnt % kStages;
-        if (!wait_bar(cx, cx.full(sv), (cnt / kStages) & 1u)) break;
-        const uint8_t* rows = smem + sv * kTileBytes + warp * 32 * 256;
-        uint32_t m01 = 0u, m23 = 0u;
+      const uint32_t sv = c2 % kStages;
+      if (c2 != mine && !wait_bar(cx, cx.full(sv), (c2 / kStages) & 1u)) break;
+      const uint8_t* vr = smem + sv * kTileBytes + tw * 32 * 256;
+      uint32_t m01 = 0u, m23 = 0u;
 #pragma unroll 8
-        for (int t = 0; t < 32; ++t) {
-          if (t < nvalid) {
-            const uint2 w = tok(rows, t, lane);
-            m01 = __vmaxu2(m01, w.x & 0x7FFF7FFFu);
-            m23 = __vmaxu2(m23, w.y & 0x7FFF7FFFu);
-          }
+      for (int t = 0; t < 32; ++t) {
+        if (t < nvalid) {
+          const uint2 w = tok(vr, t, lane);
+          m01 = __vmaxu2(m01, w.x & 0x7FFF7FFFu);
+          m23 = __vmaxu2(m23, w.y & 0x7FFF7FFFu);
         }
-        tc::mbar_arrive(cx.empty(sv));
-        ++cnt;
-        vm[warp][2 * lane] = m01;
-        vm[warp][2 * lane + 1] = m23;
       }
-      compute_bar();
-      if (threadIdx.x < kHeadDim) {
-        const int c = threadIdx.x;
+      tc::mbar_arrive(cx.empty(sv));
+      vm[tw][2 * lane] = m01;
+      vm[tw][2 * lane + 1] = m23;
+      team_bar(1);
+      if (tt < kHeadDim) {
+        const int c = tt;
         const int64_t slot = (bh * G + it.g) * kHeadDim + c;
         if (prm.smooth_k) {
           // levels 1..3 of the pairwise tree over the group's 8 chunks
@@ -525,14 +556,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         prm.vmax[slot] = __uint_as_float(mb << 16);
         __threadfence();
       }
-      compute_bar();
-      if (threadIdx.x == 0) last_flag = atomicAdd(prm.done + bh, 1u) == static_cast<unsigned>(G - 1);
-      compute_bar();
+      team_bar(1);
+      if (tt == 0) last_flag = atomicAdd(prm.done + bh, 1u) == static_cast<unsigned>(G - 1);
+      team_bar(1);
       if (last_flag) {
         // finish the head: the group sums are complete (each writer fenced
         // before counting itself done)
         __threadfence();
-        const int c = threadIdx.x & (kHeadDim - 1), half = threadIdx.x >> 7;
+        const int c = tt & (kHeadDim - 1), half = tt >> 7;
         int64_t P = 1;
         while (P < G) P *= 2;
         const int64_t lo = half == 0 ? 0 : (P == 1 ? 1 : P / 2);
@@ -546,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fin_right[c] = t;
           fin_vmax[c] = vmx;
         }
-        compute_bar();
+        team_bar(1);
         if (half == 0) {
           float mu = 0.0f;
           if (prm.smooth_k) {
@@ -557,81 +588,83 @@ __global__ void __launch_bounds__(kThreads, 1)
           prm.out.v_scale[bh * kHeadDim + c] = __fdiv_rn(fmaxf(vmx, fin_vmax[c]), kE4M3Max);
           __threadfence();
         }
-        compute_bar();
-        if (threadIdx.x == 0) {
+        team_bar(1);
+        if (tt == 0) {
           asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(prm.ready + bh), "r"(1u) : "memory");
         }
       }
     } else {
-      // ----------------------------------------------------------- codes --
-      if (threadIdx.x == 0) ready_ok = wait_ready(cx, prm.ready + bh) ? 1 : 0;
-      compute_bar();
-      const bool head_ready = ready_ok != 0;
-      compute_bar();  // everyone has read ready_ok before thread 0 may write it again
+      // codes item: both tiles need the head's statistics
+      if (tt == 0) ready_ok[team] = wait_ready(cx, prm.ready + bh) ? 1 : 0;
+      team_bar(team);
+      const bool head_ready = ready_ok[team] != 0;
+      team_bar(team);  // everyone has read ready_ok before thread 0 may write it again
       if (!head_ready) break;
-      // K tile: codes of k - mean
-      float mu[4];
+      if (team == 1 && !wait_bar(cx, cx.full(mine % kStages), (mine / kStages) & 1u)) break;
+      if (team == 0) {
+        // K codes of k - mean
+        float mu[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) mu[c] = prm.smooth_k ? __ldcg(prm.out.k_mean + bh * kHeadDim + 4 * lane + c) : 0.f;
-      if (in_pad) {
-        int8_t* kc = prm.write_int8 ? prm.out.k_codes + bh * S_pad * kHeadDim : nullptr;
-        uint16_t* k16 = prm.out.k16 + bh * S_pad * kHeadDim;
-        const float skv = quantize_int8_block(tile + warp * 32 * 256, mu, nvalid, kc, k16, s0, lane);
-        if (lane == 0) prm.out.k_scale[bh * (S_pad / kQKBlock) + s0 / kQKBlock] = skv;
-      }
-      tc::mbar_arrive(cx.empty(st));
-      ++cnt;
-      // V tile: e4m3 codes, transposed to [channel][token]
-      const uint32_t sv = cnt % kStages;
-      if (!wait_bar(cx, cx.full(sv), (cnt / kStages) & 1u)) break;
-      const uint8_t* vrows = smem + sv * kTileBytes + warp * 32 * 256;
-      if (in_pad) {
-        float svs[4], rv[4];
-        bool live[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          svs[c] = __ldcg(prm.out.v_scale + bh * kHeadDim + 4 * lane + c);
-          live[c] = svs[c] > 0.0f;
-          rv[c] = svs[c] >= FLT_MIN ? __frcp_rn(svs[c]) : 0.0f;
+        for (int c = 0; c < 4; ++c)
+          mu[c] = prm.smooth_k ? __ldcg(prm.out.k_mean + bh * kHeadDim + 4 * lane + c) : 0.f;
+        if (in_pad) {
+          int8_t* kc = prm.write_int8 ? prm.out.k_codes + bh * S_pad * kHeadDim : nullptr;
+          uint16_t* k16 = prm.out.k16 + bh * S_pad * kHeadDim;
+          const float skv = quantize_int8_block(rows, mu, nvalid, kc, k16, s0, lane);
+          if (lane == 0) prm.out.k_scale[bh * (S_pad / kQKBlock) + s0 / kQKBlock] = skv;
         }
-        const bool fast01 = svs[0] >= FLT_MIN && svs[1] >= FLT_MIN;
-        const bool fast23 = svs[2] >= FLT_MIN && svs[3] >= FLT_MIN;
-        const uint32_t keep = (live[0] ? 0x000000FFu : 0u) | (live[1] ? 0x0000FF00u : 0u) |
-                              (live[2] ? 0x00FF0000u : 0u) | (live[3] ? 0xFF000000u : 0u);
-        uint32_t cw[4][8];  // cw[c][j]: tokens 4j..4j+3 of channel 4*lane+c
+        tc::mbar_arrive(cx.empty(st));
+        if (!pass(cnt + 1)) break;
+      } else {
+        // V codes, transposed to [channel][token]
+        if (in_pad) {
+          float svs[4], rv[4];
+          bool live[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint32_t a[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int t = 4 * j + q;
-            uint32_t word = 0u;
-            if (t < nvalid) {
-              const uint2 w = tok(vrows, t, lane);
-              const uint32_t p01 = v_code_pair(lo_bf16(w.x), hi_bf16(w.x), svs[0], svs[1], rv[0], rv[1], fast01);
-              const uint32_t p23 = v_code_pair(lo_bf16(w.y), hi_bf16(w.y), svs[2], svs[3], rv[2], rv[3], fast23);
-              word = (p01 | (p23 << 16)) & keep;
-            }
-            a[q] = word;
+          for (int c = 0; c < 4; ++c) {
+            svs[c] = __ldcg(prm.out.v_scale + bh * kHeadDim + 4 * lane + c);
+            live[c] = svs[c] > 0.0f;
+            rv[c] = svs[c] >= FLT_MIN ? __frcp_rn(svs[c]) : 0.0f;
           }
-          // 4x4 byte transpose: a[q] = token q's channels -> cw[c][j] = channel c's tokens
-          const uint32_t t01l = __byte_perm(a[0], a[1], 0x5140), t01h = __byte_perm(a[0], a[1], 0x7362);
-          const uint32_t t23l = __byte_perm(a[2], a[3], 0x5140), t23h = __byte_perm(a[2], a[3], 0x7362);
-          cw[0][j] = __byte_perm(t01l, t23l, 0x5410);
-          cw[1][j] = __byte_perm(t01l, t23l, 0x7632);
-          cw[2][j] = __byte_perm(t01h, t23h, 0x5410);
-          cw[3][j] = __byte_perm(t01h, t23h, 0x7632);
-        }
+          const bool fast01 = svs[0] >= FLT_MIN && svs[1] >= FLT_MIN;
+          const bool fast23 = svs[2] >= FLT_MIN && svs[3] >= FLT_MIN;
+          const uint32_t keep = (live[0] ? 0x000000FFu : 0u) | (live[1] ? 0x0000FF00u : 0u) |
+                                (live[2] ? 0x00FF0000u : 0u) | (live[3] ? 0xFF000000u : 0u);
+          uint32_t cw[4][8];  // cw[c][j]: tokens 4j..4j+3 of channel 4*lane+c
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4* dst = reinterpret_cast<uint4*>(prm.out.vt_codes + (bh * kHeadDim + 4 * lane + c) * S_pad + s0);
-          __stcs(dst, make_uint4(cw[c][0], cw[c][1], cw[c][2], cw[c][3]));
-          __stcs(dst + 1, make_uint4(cw[c][4], cw[c][5], cw[c][6], cw[c][7]));
+          for (int j = 0; j < 8; ++j) {
+            uint32_t a[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int t = 4 * j + q;
+              uint32_t word = 0u;
+              if (t < nvalid) {
+                const uint2 w = tok(rows, t, lane);
+                const uint32_t p01 = v_code_pair(lo_bf16(w.x), hi_bf16(w.x), svs[0], svs[1], rv[0], rv[1], fast01);
+                const uint32_t p23 = v_code_pair(lo_bf16(w.y), hi_bf16(w.y), svs[2], svs[3], rv[2], rv[3], fast23);
+                word = (p01 | (p23 << 16)) & keep;
+              }
+              a[q] = word;
+            }
+            // 4x4 byte transpose: a[q] = token q's channels -> cw[c][j] = channel c's tokens
+            const uint32_t t01l = __byte_perm(a[0], a[1], 0x5140), t01h = __byte_perm(a[0], a[1], 0x7362);
+            const uint32_t t23l = __byte_perm(a[2], a[3], 0x5140), t23h = __byte_perm(a[2], a[3], 0x7362);
+            cw[0][j] = __byte_perm(t01l, t23l, 0x5410);
+            cw[1][j] = __byte_perm(t01l, t23l, 0x7632);
+            cw[2][j] = __byte_perm(t01h, t23h, 0x5410);
+            cw[3][j] = __byte_perm(t01h, t23h, 0x7632);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4* dst = reinterpret_cast<uint4*>(prm.out.vt_codes + (bh * kHeadDim + 4 * lane + c) * S_pad + s0);
+            __stcs(dst, make_uint4(cw[c][0], cw[c][1], cw[c][2], cw[c][3]));
+            __stcs(dst + 1, make_uint4(cw[c][4], cw[c][5], cw[c][6], cw[c][7]));
+          }
         }
+        tc::mbar_arrive(cx.empty(mine % kStages));
       }
-      tc::mbar_arrive(cx.empty(sv));
-      ++cnt;
     }
+    cnt += n_stages;
   }
 }
 
