@@ -163,30 +163,39 @@ __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Shared-memory descriptors of the operand buffers are computed once; the
+// start-address field holds (address >> 4) in its low 14 bits and every buffer
+// lies below 256 KB, so the descriptor of buffer + offset is descriptor +
+// (offset >> 4) with no carry out of the field.
+__device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t offset) { return base + (offset >> 4); }
+
 // S_i = Q_i K^T for one 128-key tile: 8 MMAs of K = 16 over the two
-// 64-channel subtiles of the fp16 Q and K tiles. The empty asm keeps the
-// compiler from hoisting the (loop-invariant) descriptors of every buffer into
-// registers; they are recomputed from the base addresses, a few integer ops.
-__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t sbase, int i, uint32_t kst) {
-  uint32_t qa = sbase + kOffQ16 + static_cast<uint32_t>(i) * kTile16, ka = sbase + kOffK16 + kst * kTile16;
-  asm volatile("" : "+r"(qa), "+r"(ka));
+// 64-channel subtiles of the fp16 Q and K tiles (dq, dk: descriptors of the
+// two tiles' first subtiles).
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t off = static_cast<uint32_t>(ks >> 2) * kSub16 + static_cast<uint32_t>(ks & 3) * 32u;
-    tc::mma_f16_ss(tmem + col_s(i), tc::sw128_desc(qa + off), tc::sw128_desc(ka + off), tc::kIdescM128N128,
-                   ks > 0 ? 1u : 0u);
+    tc::mma_f16_ss(d_tmem, desc_at(dq, off), desc_at(dk, off), tc::kIdescM128N128, ks > 0 ? 1u : 0u);
   }
 }
 
 // O_i (+)= P_i V for one 128-key tile: 4 MMAs of K = 32; P_i (e4m3, written
 // by the softmax warps) and V^T both in shared memory, 128-byte swizzled.
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int i, uint32_t vst, bool acc) {
-  uint32_t va = sbase + kOffV + vst * kTile8, pa = sbase + kOffP + static_cast<uint32_t>(i) * kTile8;
-  asm volatile("" : "+r"(va), "+r"(pa));
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint64_t dp, uint64_t dv, bool acc) {
 #pragma unroll
   for (int ks = 0; ks < 4; ++ks)
-    tc::mma_f8_ss(tmem + col_o(i), tc::sw128_desc(pa + 32u * ks), tc::sw128_desc(va + 32u * ks),
-                  tc::kIdescM128N128, (acc || ks > 0) ? 1u : 0u);
+    tc::mma_f8_ss(d_tmem, desc_at(dp, 32u * ks), desc_at(dv, 32u * ks), tc::kIdescM128N128,
+                  (acc || ks > 0) ? 1u : 0u);
+}
+
+// One lane of the warp, chosen by the hardware (elect.sync).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // One 128-key tile of the online softmax for the calling thread's query row
@@ -395,51 +404,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp <= 2) {
       // ---------------------------------------------- MMA issuer of tile i --
-      if (lane == 0) {
-        const int i = warp - 1;
-        uint32_t k_cnt = 0, v_cnt = 0, u_cnt = 0, sf_cnt = 0, p_cnt = 0;
-        bool ok = true;
-        for (int64_t u = blockIdx.x; ok && u < prm.n_units; u += gridDim.x) {
-          if (!(ok = wait_bar(cx, cx.bar(kBarQFull), u_cnt & 1u))) break;
-          for (int64_t j = 0; ok && j <= n_kv; ++j) {
-            if (j < n_kv) {
-              // QK_j once K_j is loaded and the softmax has read S_{j-1}
-              const uint32_t ks = k_cnt % kKStages;
-              if (!(ok = wait_bar(cx, cx.bar(kBarKFull + ks), (k_cnt / kKStages) & 1u))) break;
-              if (u_cnt > 0 || j > 0) {
-                if (!(ok = wait_bar(cx, cx.bar(kBarSFree + i), sf_cnt & 1u))) break;
-                ++sf_cnt;
-              }
-              tc::tc_fence_after();
-              issue_qk(tmem, sbase, i, ks);
+      // The whole warp runs the loop (warp-uniform control flow keeps the
+      // descriptors and counters in uniform registers); one elected lane
+      // issues the MMAs and commits.
+      const int i = warp - 1;
+      const bool leader = elect_one();
+      const uint32_t d_s = tmem + col_s(i), d_o = tmem + col_o(i);
+      const uint64_t dq = tc::sw128_desc(sbase + kOffQ16 + static_cast<uint32_t>(i) * kTile16);
+      const uint64_t dk0 = tc::sw128_desc(sbase + kOffK16);
+      const uint64_t dv0 = tc::sw128_desc(sbase + kOffV);
+      const uint64_t dp = tc::sw128_desc(sbase + kOffP + static_cast<uint32_t>(i) * kTile8);
+      uint32_t k_cnt = 0, v_cnt = 0, u_cnt = 0, sf_cnt = 0, p_cnt = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < prm.n_units; u += gridDim.x) {
+        if (!(ok = wait_bar_warp(cx, cx.bar(kBarQFull), u_cnt & 1u))) break;
+        for (int64_t j = 0; ok && j <= n_kv; ++j) {
+          if (j < n_kv) {
+            // QK_j once K_j is loaded and the softmax has read S_{j-1}
+            const uint32_t ks = k_cnt % kKStages;
+            if (!(ok = wait_bar_warp(cx, cx.bar(kBarKFull + ks), (k_cnt / kKStages) & 1u))) break;
+            if (u_cnt > 0 || j > 0) {
+              if (!(ok = wait_bar_warp(cx, cx.bar(kBarSFree + i), sf_cnt & 1u))) break;
+              ++sf_cnt;
+            }
+            tc::tc_fence_after();
+            if (leader) {
+              issue_qk(d_s, dq, desc_at(dk0, ks * kTile16));
               tc::mma_commit(cx.bar(kBarSFull + i));
               tc::mma_commit(cx.bar(kBarKEmpty + ks));
-              ++k_cnt;
               if (j == n_kv - 1) tc::mma_commit(cx.bar(kBarQEmpty));
             }
-            if (j >= 1) {
-              // PV_{j-1} once P_{j-1} is in shared memory (and O rescaled)
-              const uint32_t vs = v_cnt % kVStages;
-              if (!(ok = wait_bar(cx, cx.bar(kBarVFull + vs), (v_cnt / kVStages) & 1u))) break;
-              if (!(ok = wait_bar(cx, cx.bar(kBarPFull + i), p_cnt & 1u))) break;
-              ++p_cnt;
-              if (j == 1 && !(ok = wait_bar(cx, cx.bar(kBarOEmpty + i), (u_cnt & 1u) ^ 1u))) break;
-              tc::tc_fence_after();
-              issue_pv(tmem, sbase, i, vs, j > 1);
+            __syncwarp();
+            ++k_cnt;
+          }
+          if (j >= 1) {
+            // PV_{j-1} once P_{j-1} is in shared memory (and O rescaled)
+            const uint32_t vs = v_cnt % kVStages;
+            if (!(ok = wait_bar_warp(cx, cx.bar(kBarVFull + vs), (v_cnt / kVStages) & 1u))) break;
+            if (!(ok = wait_bar_warp(cx, cx.bar(kBarPFull + i), p_cnt & 1u))) break;
+            ++p_cnt;
+            if (j == 1 && !(ok = wait_bar_warp(cx, cx.bar(kBarOEmpty + i), (u_cnt & 1u) ^ 1u))) break;
+            tc::tc_fence_after();
+            if (leader) {
+              issue_pv(d_o, dp, desc_at(dv0, vs * kTile8), j > 1);
               tc::mma_commit(cx.bar(kBarPVDone + i));
               tc::mma_commit(cx.bar(kBarVEmpty + vs));
-              ++v_cnt;
             }
+            __syncwarp();
+            ++v_cnt;
           }
-          ++u_cnt;
         }
-        // drain: all MMAs issued by this thread complete before TMEM is freed
-        tc::mma_commit(cx.bar(kBarDrain + i));
-        Ctx drain = cx;
-        volatile int no_abort = 0;
-        drain.abort_flag = &no_abort;
-        wait_bar(drain, cx.bar(kBarDrain + i), 0);
+        ++u_cnt;
       }
+      // drain: all MMAs issued by this warp complete before TMEM is freed
+      if (leader) tc::mma_commit(cx.bar(kBarDrain + i));
+      __syncwarp();
+      Ctx drain = cx;
+      volatile int no_abort = 0;
+      drain.abort_flag = &no_abort;
+      wait_bar(drain, cx.bar(kBarDrain + i), 0);
     }
     __syncwarp();
   } else {
@@ -463,9 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* ks = prm.k_scale + bh * nblk;
       float m = -INFINITY, l = 0.0f;
       float cb[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) cb[b] = cq * __ldg(ks + b);
+      // K scales of a 128-key tile: 4 consecutive floats, 16-byte aligned
+      // (S_pad / 32 is a multiple of 4)
+      float4 ks_next = __ldg(reinterpret_cast<const float4*>(ks));
       for (int64_t j = 0; j < n_kv; ++j) {
+        cb[0] = cq * ks_next.x;
+        cb[1] = cq * ks_next.y;
+        cb[2] = cq * ks_next.z;
+        cb[3] = cq * ks_next.w;
+        // the next tile's scales load while this tile is processed
+        if (j + 1 < n_kv) ks_next = __ldg(reinterpret_cast<const float4*>(ks + (j + 1) * 4));
         if (!(ok = wait_bar_warp(cx, cx.bar(kBarSFull + i), s_cnt & 1u))) break;
         ++s_cnt;
         tc::tc_fence_after();
@@ -476,10 +506,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc::tc_fence_before();
         tc::mbar_arrive(cx.bar(kBarPFull + i));
-        if (j + 1 < n_kv) {
-#pragma unroll
-          for (int b = 0; b < 4; ++b) cb[b] = cq * __ldg(ks + (j + 1) * 4 + b);
-        }
       }
       if (!ok) break;
       // epilogue: the last PV of the unit completes O; O = acc * s_v / l (l

@@ -8,8 +8,9 @@
 // opt-in (v0.4.0)", section "What changed" (64-bit offsets; key mean summed
 // in fp64).
 //
-// One persistent kernel, one CTA per SM: 8 compute warps and 1 TMA producer
-// warp. The work is a list of items claimed in order from a global counter:
+// One persistent kernel, one CTA per SM: two teams of 8 compute warps and 1
+// TMA producer warp. The work is a list of items claimed in order from a
+// global counter:
 //   stats item (head, 256-token group): Q codes and scales; exact fp64 key
 //     sums of the group (8 chunks of 32 tokens, then a 3-level pairwise tree);
 //     the group's max |v| per channel. The last stats item of a head (counted
@@ -32,8 +33,10 @@
 // summed as an unevaluated pair of floats (TwoSum: hi + lo is the exact
 // running sum while lo's own additions are exact). All values are multiples
 // of 2^L, the last-bit weight of the smallest nonzero input; with A the sum
-// of |x|, every rounding error is below 2^(e(A)-24) and lo stays exact while
-// e(A) - L <= 42. In that case every prefix sum also fits in 53 bits, so the
+// of |x|, every rounding error is below 2^(e(A)-24), and lo, which gathers
+// 33 of them (two chains of 16 tokens and the join), stays exact while
+// e(A) - L <= 42 (the float sum of |x| may sit one binade low, so the test
+// is e(fl(A)) - L <= 41). In that case every prefix sum also fits in 53 bits, so the
 // left-to-right fp64 sum equals the exact sum and hi + lo (added in fp64) is
 // bit-identical to it. Otherwise the chunk is re-summed left to right in fp64
 // from the values still held in registers.
@@ -266,7 +269,7 @@ __device__ __forceinline__ void chunk_sums(const uint8_t* rows, int nvalid, int 
     const float l = __fadd_rn(__fadd_rn(lo[0][c], lo[1][c]), err);
     const float a = __fadd_rn(am[0][c], am[1][c]);
     const int ea = static_cast<int>((__float_as_uint(a) >> 23) & 0xFFu) - 127;
-    out[c] = ea - lsb <= 40 ? __dadd_rn(static_cast<double>(s), static_cast<double>(l))
+    out[c] = ea - lsb <= 41 ? __dadd_rn(static_cast<double>(s), static_cast<double>(l))
                             : fp64_chunk_sum(rows, nvalid, lane, c);
   }
 }
