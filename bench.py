@@ -145,38 +145,43 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_sample(rows=1024, seed=3):
+def cpu_oracle_sample(rows=1024, seed=3, heads=1):
     """Times the oracle (as it stands) on a bounded sample of the workload:
-    the full prologue of one head plus the emulated attention of ``rows``
-    query rows of that head against all 16384 keys. Returns attention-op
-    throughput in TOPS over the sample and a description."""
+    for each of ``heads`` heads, the full prologue of that head plus the
+    emulated attention of ``rows`` of its query rows against all 16384 keys.
+    The step time is extrapolated to all 28 heads (the prologue's share scales
+    with heads, the attention's with query rows). Returns attention-op
+    throughput in TOPS and a description."""
     import numpy as np
-    import torch
 
     from oracle import attention_emulated, e4m3_decode, quantize_head
     from quantized_attention_fp64_gb300.workloads import WORKLOADS, make_qkv
 
     w = WORKLOADS[WORKLOAD]
     q, k, v = make_qkv(w, "cpu")
-    qh, kh, vh = (t[0, :, 0, :].float().numpy() for t in (q, k, v))
-    sel = np.sort(np.random.default_rng(seed).choice(w.S, rows, replace=False))
-    t0 = time.perf_counter()
-    r = quantize_head(qh, kh, vh, True)
-    t1 = time.perf_counter()
-    attention_emulated(r["q_codes"], r["k_codes"], e4m3_decode(r["v_codes"]), r["q_scale"], r["k_scale"],
-                       r["v_scale"], 1.0 / math.sqrt(128.0), rows=sel)
-    t2 = time.perf_counter()
-    ops = 4.0 * rows * w.S * 128
-    # the prologue's share of a step scales with heads; the attention's with rows
-    step_time = (t1 - t0) + (t2 - t1) * (w.S / rows)   # one head of one step
-    value = 4.0 * w.S * w.S * 128 / step_time / 1e12
+    t_pro = t_att = 0.0
+    for h in range(heads):
+        qh, kh, vh = (t[0, :, h, :].float().numpy() for t in (q, k, v))
+        sel = np.arange(w.S) if rows >= w.S else np.sort(
+            np.random.default_rng(seed + h).choice(w.S, rows, replace=False))
+        t0 = time.perf_counter()
+        r = quantize_head(qh, kh, vh, True)
+        t1 = time.perf_counter()
+        attention_emulated(r["q_codes"], r["k_codes"], e4m3_decode(r["v_codes"]), r["q_scale"], r["k_scale"],
+                           r["v_scale"], 1.0 / math.sqrt(128.0), rows=sel)
+        t2 = time.perf_counter()
+        t_pro += t1 - t0
+        t_att += t2 - t1
+    n_rows = min(rows, w.S)
+    head_time = (t_pro + t_att * (w.S / n_rows)) / heads   # one full head of one step
+    value = 4.0 * w.S * w.S * 128 / head_time / 1e12
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {
         "value": value, "unit": "TOPS", "cores": cores, "kind": "oracle",
-        "sample": f"one head of {WORKLOAD}: full prologue ({t1 - t0:.2f} s) + emulated attention of {rows} "
-                  f"query rows x {w.S} keys ({t2 - t1:.2f} s), scaled to the head's {w.S} rows; numpy, "
-                  f"BLAS threads up to {cores}",
-        "attention_ops_sampled": ops, "seconds": t2 - t0,
+        "sample": f"{heads} head(s) of {WORKLOAD}: full prologue ({t_pro:.2f} s) + emulated attention of "
+                  f"{n_rows} query rows x {w.S} keys per head ({t_att:.2f} s), extrapolated to the step's "
+                  f"{w.H} heads x {w.S} rows; numpy, BLAS threads up to {cores}",
+        "attention_ops_sampled": 4.0 * heads * n_rows * w.S * 128, "seconds": t_pro + t_att,
     }
 
 
@@ -367,7 +372,7 @@ def run_gpu(args):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(rows=args.ref_rows)
+        line["cpu_baseline"] = cpu_oracle_sample(rows=args.cpu_rows, heads=args.cpu_heads)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -383,7 +388,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=1024)
+    ap.add_argument("--ref-rows", type=int, default=1024, help="query rows per --impl reference step")
+    ap.add_argument("--cpu-rows", type=int, default=16384, help="query rows per head of the cpu_baseline sample")
+    ap.add_argument("--cpu-heads", type=int, default=2, help="heads of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true", help="run one prologue + attention on --workload and exit")
     ap.add_argument("--workload", default=WORKLOAD)

@@ -18,7 +18,7 @@
 //     gives the key mean, the max over groups the V scales; then it publishes
 //     the head as ready.
 //   codes item (head, 256-token group): K codes of k - mean, V codes
-//     (transposed), after waiting until the head is ready.
+//     (transposed); the producer loads its tiles once the head is ready.
 // The codes items of head h come after the stats items of head h + L, so K
 // and V are read the second time while still in L2 (L is sized from the L2
 // capacity). The producer loads each tensor's 256-token x 128-channel bf16
@@ -30,24 +30,20 @@
 //
 // Exactness of the key sum. fp64 adds run at under 2 per clock per SM on
 // this GPU, far below what the HBM stream needs, so each 32-token chunk is
-// summed as an unevaluated pair of floats (TwoSum: hi + lo is the exact
-// running sum while lo's own additions are exact). All values are multiples
-// of 2^L, the last-bit weight of the smallest nonzero input; with A the sum
-// of |x|, every rounding error is below 2^(e(A)-24), and lo, which gathers
-// 33 of them (two chains of 16 tokens and the join), stays exact while
-// e(A) - L <= 42 (the float sum of |x| may sit one binade low, so the test
-// is e(fl(A)) - L <= 41). In that case every prefix sum also fits in 53 bits, so the
-// left-to-right fp64 sum equals the exact sum and hi + lo (added in fp64) is
-// bit-identical to it. Otherwise the chunk is re-summed left to right in fp64
-// from the values still held in registers.
+// summed as unevaluated pairs of floats (TwoSum chains, two-element packed
+// arithmetic), which give the exact chunk sum whenever the spread of
+// exponents in the chunk is bounded (see chunk_sums); that exact sum is what
+// the left-to-right fp64 sum produces too, so the result is bit-identical.
+// Otherwise the chunk is summed left to right in fp64.
 //
 // Exactness of the codes. A code is rint(x / s) with x / s correctly
-// rounded. The fast path uses q = x * fl(1/s); |q - x/s| < 2^-16 and
-// |fl(x/s) - x/s| <= 2^-18 for |x/s| <= 127.5, so whenever q is farther than
-// 2^-15 from a half-integer both round to the same integer; otherwise the
-// exact division decides. For e4m3, rounding is monotone, so when q scaled by
-// (1 - 2^-21) and by (1 + 2^-21) round to the same code, fl(v/s) (within
-// 2^-22 relative of q) does too; otherwise the exact division decides.
+// rounded in fp32. The fast path multiplies by fl(1/s) and falls back to the
+// exact division whenever the product is within 2^-15 of a half-integer
+// (quantize_block). For e4m3, rounding is monotone, so when q = fl(v*fl(1/s))
+// scaled by (1 - 2^-21) and by (1 + 2^-21) round to the same code, fl(v/s)
+// (within 2^-22 relative of q) does too; otherwise the exact division
+// decides (v_code_quad). Q and V maxima are taken on the bf16 bit patterns,
+// whose magnitudes order as integers.
 #include <cuda_fp16.h>
 
 #include <cfloat>
@@ -121,11 +117,10 @@ __device__ __forceinline__ Item decode_item(int64_t i, int64_t NH, int64_t G, in
 
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// Both channels of a bf16x2 word as fp32 (exact): .x the low half, .y the high half.
+__device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(lo_bf16(w), hi_bf16(w)); }
 
-// Channel c (0..3) of a lane's 4-channel group.
-__device__ __forceinline__ float chan(const uint2& w, int c) {
-  return c == 0 ? lo_bf16(w.x) : c == 1 ? hi_bf16(w.x) : c == 2 ? lo_bf16(w.y) : hi_bf16(w.y);
-}
+constexpr uint32_t kAbs2 = 0x7FFF7FFFu;  // clears the sign bits of a bf16x2 word
 
 // Number of tokens s0 .. s0+31 that are below S.
 __device__ __forceinline__ int valid_in_chunk(int64_t S, int64_t s0) {
@@ -133,10 +128,23 @@ __device__ __forceinline__ int valid_in_chunk(int64_t S, int64_t s0) {
   return d <= 0 ? 0 : (d >= 32 ? 32 : static_cast<int>(d));
 }
 
-// Channels [4*lane, 4*lane+4) of token t of the warp's 32 tokens, from a
-// shared-memory tile of 256-byte token rows (a warp instruction reads one row).
-__device__ __forceinline__ uint2 tok(const uint8_t* rows, int t, int lane) {
+// Shared-memory tiles hold 256-byte token rows (128 bf16 channels). Two lane
+// mappings read them without bank conflicts:
+//  - 8-channel lanes: lane l reads channels 8*(l & 15) .. +8 of token
+//    2*i + (l >> 4), so one warp instruction covers two whole rows;
+//  - 4-channel lanes: lane l reads channels 4*l .. +4 of one token, one row
+//    per warp instruction (used where each lane needs all 32 tokens).
+__device__ __forceinline__ uint4 tok8(const uint8_t* rows, int t, int lane) {
+  return *reinterpret_cast<const uint4*>(rows + t * 256 + (lane & 15) * 16);
+}
+__device__ __forceinline__ uint2 tok4(const uint8_t* rows, int t, int lane) {
   return *reinterpret_cast<const uint2*>(rows + t * 256 + lane * 8);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -145,132 +153,213 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Exact path of a code: bits of fl(fl(x / s) + kMagic). Kept out of line:
-// it runs only when the fast path cannot decide.
-__device__ __noinline__ uint32_t exact_code_bits(float x, float s) {
-  return __float_as_uint(__fadd_rn(__fdiv_rn(x, s), kMagic));
-}
-
-// Bits of fl(q + kMagic) where q = fl(x / s); the low byte is the int8 code.
-__device__ __forceinline__ uint32_t int8_code_bits(float x, float s, float r, bool fast) {
-  if (fast) {
-    const float q = __fmul_rn(x, r);
-    const float t = __fadd_rn(q, kMagic);
-    const float f = __fsub_rn(q, __fsub_rn(t, kMagic));
-    if (fabsf(f) < kHalfGuard) return __float_as_uint(t);
-  }
-  return exact_code_bits(x, s);
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
-// Four int8 codes (one word) as four fp16 values, exactly: the fp16 bit
-// pattern 0x6400 | (c ^ 0x80) is 1024 + c + 128, and subtracting 1152 leaves c.
-__device__ __forceinline__ uint2 codes_to_f16x4(uint32_t w) {
-  const uint32_t x = w ^ 0x80808080u;
-  const uint32_t a = __byte_perm(x, 0x64646464u, 0x5140);
-  const uint32_t b = __byte_perm(x, 0x64646464u, 0x7362);
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-  __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
-  return make_uint2(*reinterpret_cast<uint32_t*>(&ha), *reinterpret_cast<uint32_t*>(&hb));
+// Two fp32 values (both exactly representable) as an fp16x2 word, lo in the low half.
+__device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// INT8 codes and scale of one 32-token block (the warp's rows of a shared
-// tile, 4 channels per lane), of x - mu. Writes rows s0..s0+31 of f16_bh
-// ([S_pad][128], the codes as fp16) and, when codes_bh is not null, of
-// codes_bh ([S_pad][128] int8); both with streaming stores. Returns the scale.
-__device__ __forceinline__ float quantize_int8_block(const uint8_t* rows, const float (&mu)[4], int nvalid,
-                                                     int8_t* codes_bh, uint16_t* f16_bh, int64_t s0, int lane) {
-  float a = 0.0f;
+// Exact path of a code: bits of fl(fl(x / s) + kMagic), whose low byte is
+// rint_even(fl(x / s)) as an int8. Out of line: the fast path below decides
+// all but a few codes in 10^4.
+__device__ __noinline__ uint32_t exact_code_bits(float x, float s) {
+  return __float_as_uint(__fadd_rn(__fdiv_rn(x, s), kMagic));
+}
+
+// INT8 codes and scale of one 32-token block: x (kMu false) or fl(x - mu)
+// (kMu true; nmu holds -mu for the lane's 8 channels as pairs). Reads the
+// warp's 32 rows of a shared tile with 8-channel lanes; writes rows
+// s0..s0+31 of f16_bh ([S_pad][128], the codes as fp16 values) and, when
+// codes_bh is not null, of codes_bh ([S_pad][128] int8), with streaming
+// stores; rows at or past nvalid are written as zero codes. kFull: nvalid is
+// 32. Returns the scale.
+//
+// Fast path for the codes (two-element packed arithmetic): t = fl(x*r + M)
+// with r = fl(1/s) and M = 1.5*2^23 is M + rint_even(x*r) (the spacing of
+// floats near M is 1); c = t - M exactly; g = fl(c - x*r). x*r is within
+// 2^-17 of x/s, and so is fl(x/s) (|x/s| <= 127.5), so when |g| < 1/2 - 2^-15
+// the code c is rint_even(fl(x/s)); otherwise the exact division decides.
+template <bool kMu, bool kFull>
+__device__ __forceinline__ float quantize_block(const uint8_t* rows, const float2 (&nmu)[4], int nvalid,
+                                                int8_t* codes_bh, uint16_t* f16_bh, int64_t s0, int lane) {
+  const int half = lane >> 4;
+  float a;
+  if (!kMu) {
+    // block amax on the bf16 bit patterns (magnitudes order as integers)
+    uint32_t m0 = 0u, m1 = 0u;
 #pragma unroll 8
-  for (int t = 0; t < 32; ++t) {
-    if (t < nvalid) {
-      const uint2 w = tok(rows, t, lane);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) a = fmaxf(a, fabsf(__fsub_rn(chan(w, c), mu[c])));
+    for (int i = 0; i < 16; ++i) {
+      const int t = 2 * i + half;
+      if (kFull || t < nvalid) {
+        const uint4 w = tok8(rows, t, lane);
+        m0 = __vimax3_u16x2(m0, w.x & kAbs2, w.y & kAbs2);
+        m1 = __vimax3_u16x2(m1, w.z & kAbs2, w.w & kAbs2);
+      }
     }
+    const uint32_t m = __vmaxu2(m0, m1);
+    a = __uint_as_float(warp_max_u32(max(m & 0xFFFFu, m >> 16)) << 16);
+  } else {
+    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll 8
+    for (int i = 0; i < 16; ++i) {
+      const int t = 2 * i + half;
+      if (kFull || t < nvalid) {
+        const uint4 w = tok8(rows, t, lane);
+        const float2 k0 = __fadd2_rn(bf2(w.x), nmu[0]), k1 = __fadd2_rn(bf2(w.y), nmu[1]);
+        const float2 k2 = __fadd2_rn(bf2(w.z), nmu[2]), k3 = __fadd2_rn(bf2(w.w), nmu[3]);
+        a0 = max3(a0, fabsf(k0.x), fabsf(k0.y));
+        a1 = max3(a1, fabsf(k1.x), fabsf(k1.y));
+        a0 = max3(a0, fabsf(k2.x), fabsf(k2.y));
+        a1 = max3(a1, fabsf(k3.x), fabsf(k3.y));
+      }
+    }
+    a = warp_max(fmaxf(a0, a1));
   }
-  a = warp_max(a);
   const float s = __fdiv_rn(a, kInt8Max);
   const bool fast = s >= FLT_MIN;
   const float r = fast ? __frcp_rn(s) : 0.0f;
-  uint32_t* out = codes_bh ? reinterpret_cast<uint32_t*>(codes_bh + s0 * kHeadDim) + lane : nullptr;
-  uint2* out16 = reinterpret_cast<uint2*>(f16_bh + s0 * kHeadDim) + lane;
+  const float2 r2 = make_float2(r, r), nr2 = make_float2(-r, -r);
+  const float2 m2 = make_float2(kMagic, kMagic), nm2 = make_float2(-kMagic, -kMagic);
+  uint2* out8 = codes_bh ? reinterpret_cast<uint2*>(codes_bh + s0 * kHeadDim) + (lane & 15) : nullptr;
+  uint4* out16 = reinterpret_cast<uint4*>(f16_bh + s0 * kHeadDim) + (lane & 15);
 #pragma unroll 4
-  for (int t = 0; t < 32; ++t) {
-    uint32_t word = 0u;
-    if (t < nvalid && a > 0.0f) {
-      const uint2 w = tok(rows, t, lane);
-      uint32_t bits[4];
+  for (int i = 0; i < 16; ++i) {
+    const int t = 2 * i + half;
+    uint2 c8 = make_uint2(0u, 0u);
+    uint4 c16 = make_uint4(0u, 0u, 0u, 0u);
+    if ((kFull || t < nvalid) && a > 0.0f) {
+      const uint4 w = tok8(rows, t, lane);
+      float2 x[4] = {bf2(w.x), bf2(w.y), bf2(w.z), bf2(w.w)};
+      if (kMu) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) bits[c] = int8_code_bits(__fsub_rn(chan(w, c), mu[c]), s, r, fast);
-      word = pack_low_bytes(bits[0], bits[1], bits[2], bits[3]);
+        for (int k = 0; k < 4; ++k) x[k] = __fadd2_rn(x[k], nmu[k]);
+      }
+      float2 tt[4], cc[4];
+      float g = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        tt[k] = __ffma2_rn(x[k], r2, m2);
+        cc[k] = __fadd2_rn(tt[k], nm2);
+        const float2 gk = __ffma2_rn(x[k], nr2, cc[k]);
+        g = max3(g, fabsf(gk.x), fabsf(gk.y));
+      }
+      if (!(fast && g < kHalfGuard)) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          tt[k].x = __uint_as_float(exact_code_bits(x[k].x, s));
+          tt[k].y = __uint_as_float(exact_code_bits(x[k].y, s));
+          cc[k] = __fadd2_rn(tt[k], nm2);
+        }
+      }
+      c8.x = pack_low_bytes(__float_as_uint(tt[0].x), __float_as_uint(tt[0].y), __float_as_uint(tt[1].x),
+                            __float_as_uint(tt[1].y));
+      c8.y = pack_low_bytes(__float_as_uint(tt[2].x), __float_as_uint(tt[2].y), __float_as_uint(tt[3].x),
+                            __float_as_uint(tt[3].y));
+      c16 = make_uint4(f16x2(cc[0].x, cc[0].y), f16x2(cc[1].x, cc[1].y), f16x2(cc[2].x, cc[2].y),
+                       f16x2(cc[3].x, cc[3].y));
     }
-    if (out) __stcs(out + t * (kHeadDim / 4), word);
-    __stcs(out16 + t * (kHeadDim / 4), codes_to_f16x4(word));
+    if (out8) __stcs(out8 + t * (kHeadDim / 8), c8);
+    __stcs(out16 + t * (kHeadDim / 8), c16);
   }
   return s;
 }
 
-// Left-to-right fp64 sum of channel c over the first nvalid rows (the exact
-// reference order, used when the float-pair path cannot guarantee it).
-__device__ __noinline__ double fp64_chunk_sum(const uint8_t* rows, int nvalid, int lane, int c) {
+// Left-to-right fp64 sum of one channel (byte offset `cb` in a row) over the
+// first nvalid rows: the reference order, used when the float-pair path
+// cannot guarantee it.
+__device__ __noinline__ double fp64_chunk_sum(const uint8_t* rows, int nvalid, int cb) {
   double p = 0.0;
-  for (int t = 0; t < nvalid; ++t) p = __dadd_rn(p, static_cast<double>(chan(tok(rows, t, lane), c)));
+  for (int t = 0; t < nvalid; ++t)
+    p = __dadd_rn(p, static_cast<double>(
+                         __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rows + t * 256 + cb))
+                                         << 16)));
   return p;
 }
 
-// Exact fp64 chunk sums of the lane's 4 channels over the warp's rows (see
-// the file comment for why the float-pair path is bit-identical). Even and
-// odd tokens run in two float-pair chains for instruction-level parallelism;
-// joining them adds one more error term to lo, inside the same bound.
-__device__ __forceinline__ void chunk_sums(const uint8_t* rows, int nvalid, int lane, double (&out)[4]) {
-  float hi[2][4], lo[2][4], am[2][4];
+// Exact fp64 sums of one 32-token chunk for the lane's 8 channels (8-channel
+// lanes; results valid in every lane, for channels 8*(lane & 15) .. +8).
+//
+// Each half-warp runs one float-pair chain per channel over its 16 tokens
+// (TwoSum: hi + lo stays the exact running sum while lo's own additions are
+// exact); the two chains are joined across the half-warps with one more
+// TwoSum. Exactness: every input is a multiple of 2^L, L the last-bit weight
+// of the smallest nonzero magnitude in the lane's channels; with E the
+// exponent of the largest magnitude, every partial sum is below 32 * 2^(E+1)
+// = 2^(E+6) in magnitude, so every TwoSum error is a multiple of 2^L below
+// 2^(E-19), and lo, which adds 33 of them, stays below 2^(E-13). lo's sums
+// are therefore exact in fp32 while E - 13 <= L + 24; the code takes the fast
+// result when E - L <= 36. The exact total T = hi + lo is then a multiple of
+// 2^L below 2^(E+6) and fits in 53 bits, as does every prefix of the
+// left-to-right fp64 sum, which is therefore exact too and equals T;
+// fl64(hi + lo) = T. Otherwise the chunk is summed left to right in fp64.
+template <bool kFull>
+__device__ __forceinline__ void chunk_sums(const uint8_t* rows, int nvalid, int lane, double (&out)[8]) {
+  const int half = lane >> 4;
+  const float2 neg1 = make_float2(-1.0f, -1.0f);
+  float2 hi[4], lo[4];
 #pragma unroll
-  for (int k = 0; k < 2; ++k)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) hi[k][c] = lo[k][c] = am[k][c] = 0.0f;
-  uint32_t umin = 0xFFFFFFFFu;  // (|bits| - 1) of the smallest nonzero magnitude; zeros wrap to all-ones
+  for (int k = 0; k < 4; ++k) hi[k] = lo[k] = make_float2(0.0f, 0.0f);
+  uint32_t mx0 = 0u, mx1 = 0u;                 // largest magnitude bits, per 16-bit half
+  uint32_t mn0 = 0xFFFFFFFFu, mn1 = 0xFFFFFFFFu;  // (magnitude bits - 1); zeros wrap to 0xFFFF
 #pragma unroll 4
-  for (int t = 0; t < 32; t += 2) {
+  for (int i = 0; i < 16; ++i) {
+    const int t = 2 * i + half;
+    if (kFull || t < nvalid) {
+      const uint4 w = tok8(rows, t, lane);
+      const uint32_t a0 = w.x & kAbs2, a1 = w.y & kAbs2, a2 = w.z & kAbs2, a3 = w.w & kAbs2;
+      mx0 = __vimax3_u16x2(mx0, a0, a1);
+      mx1 = __vimax3_u16x2(mx1, a2, a3);
+      mn0 = __vimin3_u16x2(mn0, __vsub2(a0, 0x00010001u), __vsub2(a1, 0x00010001u));
+      mn1 = __vimin3_u16x2(mn1, __vsub2(a2, 0x00010001u), __vsub2(a3, 0x00010001u));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (t + k < nvalid) {
-        const uint2 w = tok(rows, t + k, lane);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float x = chan(w, c);
-          const float s = __fadd_rn(hi[k][c], x);
-          const float bb = __fsub_rn(s, hi[k][c]);
-          const float err = __fadd_rn(__fsub_rn(hi[k][c], __fsub_rn(s, bb)), __fsub_rn(x, bb));
-          hi[k][c] = s;
-          lo[k][c] = __fadd_rn(lo[k][c], err);
-          am[k][c] = __fadd_rn(am[k][c], fabsf(x));
-        }
-        umin = min(umin, (w.x & 0x7FFFu) - 1u);
-        umin = min(umin, ((w.x >> 16) & 0x7FFFu) - 1u);
-        umin = min(umin, (w.y & 0x7FFFu) - 1u);
-        umin = min(umin, ((w.y >> 16) & 0x7FFFu) - 1u);
+      for (int k = 0; k < 4; ++k) {
+        const float2 x = bf2(ws[k]);
+        const float2 sum = __fadd2_rn(hi[k], x);
+        const float2 bb = __ffma2_rn(hi[k], neg1, sum);                       // sum - hi
+        const float2 t2 = __ffma2_rn(__ffma2_rn(bb, neg1, sum), neg1, hi[k]);  // hi - (sum - bb)
+        const float2 t3 = __ffma2_rn(bb, neg1, x);                             // x - bb
+        hi[k] = sum;
+        lo[k] = __fadd2_rn(lo[k], __fadd2_rn(t2, t3));
       }
     }
   }
-  int ef = static_cast<int>(((umin + 1u) >> 7) & 0xFFu);
-  if (ef == 0) ef = 1;                 // subnormal bf16: last-bit weight 2^-133
-  const int lsb = ef - 127 - 7;         // L: exponent of the smallest last-bit weight
+  // join the two half-warps' chains (both halves compute the same result)
+  uint32_t mx = __vmaxu2(mx0, mx1), mn = __vminu2(mn0, mn1);
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
+  const uint32_t mxb = max(mx & 0xFFFFu, mx >> 16);
+  const uint32_t mnb = min(mn & 0xFFFFu, mn >> 16) + 1u;  // 0x10000 when every value is zero
+  int ef_min = static_cast<int>((mnb >> 7) & 0xFFu);
+  if (ef_min == 0) ef_min = 1;  // subnormal bf16: last-bit weight 2^-133
+  int ef_max = static_cast<int>(mxb >> 7);
+  if (ef_max == 0) ef_max = 1;
+  const bool exact = mnb > 0x7FFFu || ef_max - ef_min <= 36 - 7;  // E - L = (ef_max - ef_min) + 7
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    // join the chains: TwoSum of the high parts, the error joins lo
-    const float s = __fadd_rn(hi[0][c], hi[1][c]);
-    const float bb = __fsub_rn(s, hi[0][c]);
-    const float err = __fadd_rn(__fsub_rn(hi[0][c], __fsub_rn(s, bb)), __fsub_rn(hi[1][c], bb));
-    const float l = __fadd_rn(__fadd_rn(lo[0][c], lo[1][c]), err);
-    const float a = __fadd_rn(am[0][c], am[1][c]);
-    const int ea = static_cast<int>((__float_as_uint(a) >> 23) & 0xFFu) - 127;
-    out[c] = ea - lsb <= 41 ? __dadd_rn(static_cast<double>(s), static_cast<double>(l))
-                            : fp64_chunk_sum(rows, nvalid, lane, c);
+  for (int k = 0; k < 4; ++k) {
+    const float2 ohi = make_float2(__shfl_xor_sync(0xffffffffu, hi[k].x, 16), __shfl_xor_sync(0xffffffffu, hi[k].y, 16));
+    const float2 olo = make_float2(__shfl_xor_sync(0xffffffffu, lo[k].x, 16), __shfl_xor_sync(0xffffffffu, lo[k].y, 16));
+    const float2 sum = __fadd2_rn(hi[k], ohi);
+    const float2 bb = __ffma2_rn(hi[k], neg1, sum);
+    const float2 t2 = __ffma2_rn(__ffma2_rn(bb, neg1, sum), neg1, hi[k]);
+    const float2 t3 = __ffma2_rn(bb, neg1, ohi);
+    const float2 l = __fadd2_rn(__fadd2_rn(lo[k], olo), __fadd2_rn(t2, t3));
+    out[2 * k] = __dadd_rn(static_cast<double>(sum.x), static_cast<double>(l.x));
+    out[2 * k + 1] = __dadd_rn(static_cast<double>(sum.y), static_cast<double>(l.y));
+  }
+  if (!exact) {
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) out[c] = fp64_chunk_sum(rows, nvalid, (lane & 15) * 16 + 2 * c);
   }
 }
 
@@ -281,21 +370,27 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return r;
 }
 
-// Exact path of two V codes (out of line: rare).
-__device__ __noinline__ uint32_t exact_v_pair(float x0, float x1, float s0, float s1) {
-  return e4m3x2(__fdiv_rn(x1, s1), __fdiv_rn(x0, s0));
+// Exact path of four V codes (out of line: rare); low byte = channel 0.
+__device__ __noinline__ uint32_t exact_v_quad(uint2 w, float4 s) {
+  const uint32_t p01 = e4m3x2(__fdiv_rn(hi_bf16(w.x), s.y), __fdiv_rn(lo_bf16(w.x), s.x));
+  const uint32_t p23 = e4m3x2(__fdiv_rn(hi_bf16(w.y), s.w), __fdiv_rn(lo_bf16(w.y), s.z));
+  return p01 | (p23 << 16);
 }
 
-// Codes of channels (x0, x1) as a 16-bit pair, low byte = x0.
-__device__ __forceinline__ uint32_t v_code_pair(float x0, float x1, float s0, float s1, float r0, float r1,
-                                                bool fast) {
-  if (fast) {
-    const float q0 = __fmul_rn(x0, r0), q1 = __fmul_rn(x1, r1);
-    const uint32_t dn = e4m3x2(__fmul_rn(q1, kDn), __fmul_rn(q0, kDn));
-    const uint32_t up = e4m3x2(__fmul_rn(q1, kUp), __fmul_rn(q0, kUp));
-    if (dn == up) return dn;
-  }
-  return exact_v_pair(x0, x1, s0, s1);
+// V codes of one token's 4 channels (4-channel lanes), low byte = channel 0.
+// Rounding to e4m3 is monotone, and fl(v / s) lies within 2^-22 relative of
+// q = fl(v * fl(1/s)); so when q * (1 - 2^-21) and q * (1 + 2^-21) round to
+// the same code, that is the code of fl(v / s); otherwise the exact division
+// decides.
+__device__ __forceinline__ uint32_t v_code_quad(uint2 w, float2 r01, float2 r23, float4 s, bool fast) {
+  const float2 q01 = __fmul2_rn(bf2(w.x), r01), q23 = __fmul2_rn(bf2(w.y), r23);
+  const float2 dn = make_float2(kDn, kDn), up = make_float2(kUp, kUp);
+  const float2 d01 = __fmul2_rn(q01, dn), u01 = __fmul2_rn(q01, up);
+  const float2 d23 = __fmul2_rn(q23, dn), u23 = __fmul2_rn(q23, up);
+  const uint32_t cd = e4m3x2(d01.y, d01.x) | (e4m3x2(d23.y, d23.x) << 16);
+  const uint32_t cu = e4m3x2(u01.y, u01.x) | (e4m3x2(u23.y, u23.x) << 16);
+  if (fast && cd == cu) return cd;
+  return exact_v_quad(w, s);
 }
 
 // Pairwise tree (padded with +0.0 to a power of two) over `n` group sums
@@ -385,7 +480,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float fin_vmax[kHeadDim];
   __shared__ double fin_right[kHeadDim];
   __shared__ int last_flag;  // stats items: this CTA finished the head
-  __shared__ int ready_ok[kTeams];  // codes items: the head's statistics are published
   const uint32_t sbase = tc::smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t* meta_item = reinterpret_cast<int64_t*>(smem + kOffMeta);             // [kStages]
@@ -427,6 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (prm.smooth_k) tensors[nt++] = kTensorK;
             tensors[nt++] = kTensorV;
           } else {
+            // a codes item needs the head's key mean and V scales: its tiles
+            // enter the ring only once they are published
+            if (!(ok = wait_ready(cx, prm.ready + it.bh))) break;
             tensors[nt++] = kTensorK;
             tensors[nt++] = kTensorV;
           }
@@ -473,6 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // teams wait on every stage in ring order, so a parity wait never meets a
   // barrier two phases behind; a team releases the stages it does not use as
   // soon as they are full, and a stage is refilled once both have released it.
+  // The tiles of a codes item enter the ring only after the producer has seen
+  // the head's statistics published, so the compute warps never wait for them.
   const int team = warp / kWarps, tw = warp % kWarps, tt = threadIdx.x % kGroup;
   const int64_t S = prm.S, S_pad = prm.S_pad, G = prm.G;
   uint32_t cnt = 0;
@@ -501,10 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (team == 0 && it.phase == 0) {
       // Q codes and scale
       if (in_pad) {
-        const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-        const float s = quantize_int8_block(rows, zero, nvalid,
-                                            prm.write_int8 ? prm.out.q_codes + bh * S_pad * kHeadDim : nullptr,
-                                            prm.out.q16 + bh * S_pad * kHeadDim, s0, lane);
+        const float2 nz[4] = {};
+        int8_t* qc = prm.write_int8 ? prm.out.q_codes + bh * S_pad * kHeadDim : nullptr;
+        uint16_t* q16 = prm.out.q16 + bh * S_pad * kHeadDim;
+        const float s = nvalid == 32 ? quantize_block<false, true>(rows, nz, 32, qc, q16, s0, lane)
+                                     : quantize_block<false, false>(rows, nz, nvalid, qc, q16, s0, lane);
         if (lane == 0) prm.out.q_scale[bh * (S_pad / kQKBlock) + s0 / kQKBlock] = s;
       }
       tc::mbar_arrive(cx.empty(st));
@@ -515,29 +615,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t c2 = mine;
       if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
       if (prm.smooth_k) {
-        double sums[4];
-        chunk_sums(rows, nvalid, lane, sums);
+        double sums[8];
+        if (nvalid == 32)
+          chunk_sums<true>(rows, 32, lane, sums);
+        else
+          chunk_sums<false>(rows, nvalid, lane, sums);
         tc::mbar_arrive(cx.empty(c2 % kStages));
         ++c2;
+        if (lane < 16) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ks[tw][4 * lane + c] = sums[c];
+          for (int c = 0; c < 8; ++c) ks[tw][8 * lane + c] = sums[c];
+        }
       }
       // V tile: max |v| per channel (bf16 magnitudes compare as integers)
       const uint32_t sv = c2 % kStages;
       if (c2 != mine && !wait_bar(cx, cx.full(sv), (c2 / kStages) & 1u)) break;
       const uint8_t* vr = smem + sv * kTileBytes + tw * 32 * 256;
-      uint32_t m01 = 0u, m23 = 0u;
-#pragma unroll 8
-      for (int t = 0; t < 32; ++t) {
-        if (t < nvalid) {
-          const uint2 w = tok(vr, t, lane);
-          m01 = __vmaxu2(m01, w.x & 0x7FFF7FFFu);
-          m23 = __vmaxu2(m23, w.y & 0x7FFF7FFFu);
+      const int half = lane >> 4;
+      uint32_t m4[4] = {0u, 0u, 0u, 0u};  // channel pairs (8l, 8l+1) .. (8l+6, 8l+7)
+      if (nvalid == 32) {
+#pragma unroll 4
+        for (int i = 0; i < 8; ++i) {
+          const uint4 wa = tok8(vr, 4 * i + half, lane), wb = tok8(vr, 4 * i + 2 + half, lane);
+          m4[0] = __vimax3_u16x2(m4[0], wa.x & kAbs2, wb.x & kAbs2);
+          m4[1] = __vimax3_u16x2(m4[1], wa.y & kAbs2, wb.y & kAbs2);
+          m4[2] = __vimax3_u16x2(m4[2], wa.z & kAbs2, wb.z & kAbs2);
+          m4[3] = __vimax3_u16x2(m4[3], wa.w & kAbs2, wb.w & kAbs2);
+        }
+      } else {
+        for (int i = 0; i < 16; ++i) {
+          const int t = 2 * i + half;
+          if (t < nvalid) {
+            const uint4 w = tok8(vr, t, lane);
+            m4[0] = __vmaxu2(m4[0], w.x & kAbs2);
+            m4[1] = __vmaxu2(m4[1], w.y & kAbs2);
+            m4[2] = __vmaxu2(m4[2], w.z & kAbs2);
+            m4[3] = __vmaxu2(m4[3], w.w & kAbs2);
+          }
         }
       }
       tc::mbar_arrive(cx.empty(sv));
-      vm[tw][2 * lane] = m01;
-      vm[tw][2 * lane + 1] = m23;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m4[k] = __vmaxu2(m4[k], __shfl_xor_sync(0xffffffffu, m4[k], 16));
+      if (lane < 16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) vm[tw][4 * lane + k] = m4[k];
+      }
       team_bar(1);
       if (tt < kHeadDim) {
         const int c = tt;
@@ -597,42 +720,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      // codes item: both tiles need the head's statistics
-      if (tt == 0) ready_ok[team] = wait_ready(cx, prm.ready + bh) ? 1 : 0;
-      team_bar(team);
-      const bool head_ready = ready_ok[team] != 0;
-      team_bar(team);  // everyone has read ready_ok before thread 0 may write it again
-      if (!head_ready) break;
+      // codes item (the head's key mean and V scales are published)
       if (team == 1 && !wait_bar(cx, cx.full(mine % kStages), (mine / kStages) & 1u)) break;
       if (team == 0) {
         // K codes of k - mean
-        float mu[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          mu[c] = prm.smooth_k ? __ldcg(prm.out.k_mean + bh * kHeadDim + 4 * lane + c) : 0.f;
         if (in_pad) {
           int8_t* kc = prm.write_int8 ? prm.out.k_codes + bh * S_pad * kHeadDim : nullptr;
           uint16_t* k16 = prm.out.k16 + bh * S_pad * kHeadDim;
-          const float skv = quantize_int8_block(rows, mu, nvalid, kc, k16, s0, lane);
+          float skv;
+          if (prm.smooth_k) {
+            const float4* mp = reinterpret_cast<const float4*>(prm.out.k_mean + bh * kHeadDim + 8 * (lane & 15));
+            const float4 ma = __ldcg(mp), mb = __ldcg(mp + 1);
+            const float2 nmu[4] = {make_float2(-ma.x, -ma.y), make_float2(-ma.z, -ma.w), make_float2(-mb.x, -mb.y),
+                                   make_float2(-mb.z, -mb.w)};
+            skv = nvalid == 32 ? quantize_block<true, true>(rows, nmu, 32, kc, k16, s0, lane)
+                               : quantize_block<true, false>(rows, nmu, nvalid, kc, k16, s0, lane);
+          } else {
+            const float2 nz[4] = {};
+            skv = nvalid == 32 ? quantize_block<false, true>(rows, nz, 32, kc, k16, s0, lane)
+                               : quantize_block<false, false>(rows, nz, nvalid, kc, k16, s0, lane);
+          }
           if (lane == 0) prm.out.k_scale[bh * (S_pad / kQKBlock) + s0 / kQKBlock] = skv;
         }
         tc::mbar_arrive(cx.empty(st));
         if (!pass(cnt + 1)) break;
       } else {
-        // V codes, transposed to [channel][token]
+        // V codes, transposed to [channel][token] (4-channel lanes)
         if (in_pad) {
-          float svs[4], rv[4];
-          bool live[4];
+          const float4 svs = __ldcg(reinterpret_cast<const float4*>(prm.out.v_scale + bh * kHeadDim + 4 * lane));
+          const float sc[4] = {svs.x, svs.y, svs.z, svs.w};
+          float rv[4];
+          uint32_t keep = 0u;
+          bool fast = true;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            svs[c] = __ldcg(prm.out.v_scale + bh * kHeadDim + 4 * lane + c);
-            live[c] = svs[c] > 0.0f;
-            rv[c] = svs[c] >= FLT_MIN ? __frcp_rn(svs[c]) : 0.0f;
+            rv[c] = sc[c] >= FLT_MIN ? __frcp_rn(sc[c]) : 0.0f;
+            if (sc[c] > 0.0f) keep |= 0xFFu << (8 * c);
+            fast = fast && (sc[c] >= FLT_MIN || sc[c] == 0.0f);  // zero channels are masked to code 0
           }
-          const bool fast01 = svs[0] >= FLT_MIN && svs[1] >= FLT_MIN;
-          const bool fast23 = svs[2] >= FLT_MIN && svs[3] >= FLT_MIN;
-          const uint32_t keep = (live[0] ? 0x000000FFu : 0u) | (live[1] ? 0x0000FF00u : 0u) |
-                                (live[2] ? 0x00FF0000u : 0u) | (live[3] ? 0xFF000000u : 0u);
+          const float2 r01 = make_float2(rv[0], rv[1]), r23 = make_float2(rv[2], rv[3]);
           uint32_t cw[4][8];  // cw[c][j]: tokens 4j..4j+3 of channel 4*lane+c
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -640,14 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int t = 4 * j + q;
-              uint32_t word = 0u;
-              if (t < nvalid) {
-                const uint2 w = tok(rows, t, lane);
-                const uint32_t p01 = v_code_pair(lo_bf16(w.x), hi_bf16(w.x), svs[0], svs[1], rv[0], rv[1], fast01);
-                const uint32_t p23 = v_code_pair(lo_bf16(w.y), hi_bf16(w.y), svs[2], svs[3], rv[2], rv[3], fast23);
-                word = (p01 | (p23 << 16)) & keep;
-              }
-              a[q] = word;
+              a[q] = (nvalid == 32 || t < nvalid) ? v_code_quad(tok4(rows, t, lane), r01, r23, svs, fast) & keep : 0u;
             }
             // 4x4 byte transpose: a[q] = token q's channels -> cw[c][j] = channel c's tokens
             const uint32_t t01l = __byte_perm(a[0], a[1], 0x5140), t01h = __byte_perm(a[0], a[1], 0x7362);

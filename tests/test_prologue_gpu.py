@@ -76,3 +76,28 @@ def test_prologue_edge_values(sage_lib):
     qt, kt, vt = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (q, k, v))
     for smooth in (True, False):
         _run(qt, kt, vt, "NHD", smooth)
+
+
+def test_prologue_key_sum_exponent_spread(sage_lib):
+    """Key chunks whose magnitudes span 20 to 50 binades, so that both the
+    float-pair chunk sums and the fp64 fallback run, with cancelling signs and
+    ragged chunks; the key mean and every code must still match bit for bit."""
+    rng = np.random.default_rng(11)
+    S, H = 1000, 3
+    q = rng.standard_normal((1, S, H, 128)).astype(np.float32)
+    k = rng.standard_normal((1, S, H, 128)).astype(np.float32)
+    v = rng.standard_normal((1, S, H, 128)).astype(np.float32)
+    for c in range(128):
+        spread = 20 + (c % 31)                     # exponent gap between big and tiny entries
+        for chunk in range(0, S, 32):
+            rows = slice(chunk, min(chunk + 32, S))
+            n = min(32, S - chunk)
+            sign = rng.choice([-1.0, 1.0], n)
+            big = rng.integers(0, n)
+            vals = sign * np.ldexp(rng.uniform(1, 2, n), -spread)
+            vals[big] = sign[big] * rng.uniform(1, 2) * 2.0 ** rng.integers(-2, 3)
+            k[0, rows, c % H, c] = vals
+    dev = torch.device("cuda")
+    qt, kt, vt = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (q, k, v))
+    _run(qt, kt, vt, "NHD", True)
+    _run(qt, kt, vt, "NHD", False)
