@@ -11,7 +11,6 @@ namespace sage {
 constexpr int kHeadDim = 128;     // the only supported head dimension
 constexpr int kQKBlock = 32;      // tokens per Q/K scale block ("per 32-row block")
 constexpr int kKeyTile = 128;     // keys per online-softmax step; S is padded to this
-constexpr int kGroup = 256;       // tokens per prologue CTA (8 warps x 32 tokens)
 constexpr float kInt8Max = 127.0f;
 constexpr float kE4M3Max = 448.0f;  // largest finite e4m3fn magnitude
 constexpr float kPScale = 448.0f;   // p in [0,1] is stored as e4m3(448 p)

@@ -11,39 +11,41 @@
 // One persistent kernel, one CTA per SM: two teams of 8 compute warps and 1
 // TMA producer warp. The work is a list of items claimed in order from a
 // global counter:
-//   stats item (head, 256-token group): Q codes and scales; exact fp64 key
-//     sums of the group (8 chunks of 32 tokens, then a 3-level pairwise tree);
+//   stats item (head, 128-token group): Q codes and scales; exact fp64 key
+//     sums of the group (4 chunks of 32 tokens, then a 2-level pairwise tree);
 //     the group's max |v| per channel. The last stats item of a head (counted
 //     with an atomic) finishes that head: the pairwise tree over its group sums
 //     gives the key mean, the max over groups the V scales; then it publishes
 //     the head as ready.
-//   codes item (head, 256-token group): K codes of k - mean, V codes
+//   codes item (head, 128-token group): K codes of k - mean, V codes
 //     (transposed); the producer loads its tiles once the head is ready.
 // The codes items of head h come after the stats items of head h + L, so K
 // and V are read the second time while still in L2 (L is sized from the L2
-// capacity). The producer loads each tensor's 256-token x 128-channel bf16
-// tile with one 4-D TMA copy into a 3-stage ring (64 KB per stage), so the
-// compute warps always have the next tiles in flight. Items are claimed in a
-// global order and every CTA processes its items in claim order, so the
-// stats items a codes item waits for were all claimed earlier and always
-// progress: the waits end. They are bounded anyway.
+// capacity). The producer loads each tensor's 128-token x 128-channel bf16
+// tile with one 4-D TMA copy into a 6-stage ring (32 KB per stage); an item
+// takes 2 or 3 stages, so the next items' tiles load while one is computed.
+// Two warps share each 32-token block (16 tokens each) and exchange partial
+// maxima and sums through shared memory. Items are claimed in a global order
+// and every CTA processes its items in claim order, so the stats items a
+// codes item waits for were all claimed earlier and always progress: the
+// waits end. They are bounded anyway.
 //
 // Exactness of the key sum. fp64 adds run at under 2 per clock per SM on
 // this GPU, far below what the HBM stream needs, so each 32-token chunk is
 // summed as unevaluated pairs of floats (TwoSum chains, two-element packed
 // arithmetic), which give the exact chunk sum whenever the spread of
-// exponents in the chunk is bounded (see chunk_sums); that exact sum is what
-// the left-to-right fp64 sum produces too, so the result is bit-identical.
-// Otherwise the chunk is summed left to right in fp64.
+// exponents in the chunk is bounded (see key_sum_partial); that exact sum is
+// what the left-to-right fp64 sum produces too, so the result is
+// bit-identical. Otherwise the chunk is summed left to right in fp64.
 //
 // Exactness of the codes. A code is rint(x / s) with x / s correctly
 // rounded in fp32. The fast path multiplies by fl(1/s) and falls back to the
 // exact division whenever the product is within 2^-15 of a half-integer
-// (quantize_block). For e4m3, rounding is monotone, so when q = fl(v*fl(1/s))
-// scaled by (1 - 2^-21) and by (1 + 2^-21) round to the same code, fl(v/s)
-// (within 2^-22 relative of q) does too; otherwise the exact division
-// decides (v_code_quad). Q and V maxima are taken on the bf16 bit patterns,
-// whose magnitudes order as integers.
+// (quantize_half_block). For e4m3, rounding is monotone, so when
+// q = fl(v*fl(1/s)) scaled by (1 - 2^-21) and by (1 + 2^-21) round to the same
+// code, fl(v/s) (within 2^-22 relative of q) does too; otherwise the exact
+// division decides (v_code_quad). Q and V maxima are taken on the bf16 bit
+// patterns, whose magnitudes order as integers.
 #include <cuda_fp16.h>
 
 #include <cfloat>
@@ -54,23 +56,38 @@
 namespace sage {
 namespace {
 
-constexpr int kWarps = kGroup / 32;            // 8 compute warps
-constexpr int kTeams = 2;                      // compute teams of kWarps warps
-constexpr int kThreads = kTeams * kGroup + 32; // + the producer warp
-constexpr int kStages = 3;
-constexpr uint32_t kTileBytes = kGroup * kHeadDim * 2;  // one bf16 tile: 256 tokens x 128 channels
+constexpr int kItemTokens = 128;                // tokens of one item (one group)
+constexpr int kChunks = kItemTokens / kQKBlock; // 32-token chunks per item
+constexpr int kWarps = 8;                       // compute warps per team
+constexpr int kHalfRows = 16;                   // tokens per warp (two warps per chunk)
+constexpr int kTeamThreads = kWarps * 32;
+constexpr int kTeams = 2;
+constexpr int kThreads = kTeams * kTeamThreads + 64;  // + the producer and the counter warp
+constexpr int kStages = 6;
+constexpr uint32_t kTileBytes = kItemTokens * kHeadDim * 2;  // one bf16 tile: 128 tokens x 128 channels
 constexpr float kMagic = 12582912.0f;          // 1.5 * 2^23: q + kMagic = rint_even(q) + kMagic for |q| < 2^22
 constexpr float kHalfGuard = 0.5f - 0x1p-15f;  // fast-path guard for rint
 constexpr float kDn = 1.0f - 0x1p-21f;
 constexpr float kUp = 1.0f + 0x1p-21f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+static_assert(kChunks * 2 == kWarps, "two warps per 32-token chunk");
 
-enum : int { kTensorQ = 0, kTensorK = 1, kTensorV = 2, kEnd = 3 };
+// ring entries: a tile of one tensor, a marker to finish a head, the end
+enum : int { kTensorQ = 0, kTensorK = 1, kTensorV = 2, kFinish = 3, kEnd = 4 };
+constexpr int kEvents = 8;   // ring of "group done" events from team 1 to the producer
+constexpr int kFinCap = 32;  // heads waiting for their finish marker (see the producer)
 
-// shared memory: kStages tiles, then the barriers and per-stage item tags
-constexpr uint32_t kOffBar = kStages * kTileBytes;
-constexpr uint32_t kOffMeta = kOffBar + 2 * kStages * 8;
-constexpr uint32_t kOffFlags = kOffMeta + kStages * 16;
+// shared memory: kStages tiles; per stage the head statistics a codes item
+// needs (key mean and V scales, 1 KB); the barriers; per-stage item tags;
+// the event ring and the finish queue
+constexpr uint32_t kOffHstat = kStages * kTileBytes;
+constexpr uint32_t kHstatBytes = 2 * kHeadDim * 4;
+constexpr uint32_t kOffBar = kOffHstat + kStages * kHstatBytes;
+constexpr int kNumBars = 2 * kStages + 2 * kEvents;  // full, empty, event full, event empty
+constexpr uint32_t kOffMeta = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffEvt = kOffMeta + kStages * 16;
+constexpr uint32_t kOffFinQ = kOffEvt + kEvents * 8;
+constexpr uint32_t kOffFlags = kOffFinQ + kFinCap * 8;  // abort flag, finish-queue tail, groups counted
 constexpr uint32_t kSmemBytes = kOffFlags + 16 + 1024;  // + alignment slack
 
 struct Params {
@@ -122,10 +139,10 @@ __device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(lo_bf16(w
 
 constexpr uint32_t kAbs2 = 0x7FFF7FFFu;  // clears the sign bits of a bf16x2 word
 
-// Number of tokens s0 .. s0+31 that are below S.
-__device__ __forceinline__ int valid_in_chunk(int64_t S, int64_t s0) {
+// Number of tokens s0 .. s0+n-1 that are below S.
+__device__ __forceinline__ int valid_rows(int64_t S, int64_t s0, int n) {
   const int64_t d = S - s0;
-  return d <= 0 ? 0 : (d >= 32 ? 32 : static_cast<int>(d));
+  return d <= 0 ? 0 : (d >= n ? n : static_cast<int>(d));
 }
 
 // Shared-memory tiles hold 256-byte token rows (128 bf16 channels). Two lane
@@ -133,7 +150,7 @@ __device__ __forceinline__ int valid_in_chunk(int64_t S, int64_t s0) {
 //  - 8-channel lanes: lane l reads channels 8*(l & 15) .. +8 of token
 //    2*i + (l >> 4), so one warp instruction covers two whole rows;
 //  - 4-channel lanes: lane l reads channels 4*l .. +4 of one token, one row
-//    per warp instruction (used where each lane needs all 32 tokens).
+//    per warp instruction (used where each lane needs every token).
 __device__ __forceinline__ uint4 tok8(const uint8_t* rows, int t, int lane) {
   return *reinterpret_cast<const uint4*>(rows + t * 256 + (lane & 15) * 16);
 }
@@ -169,6 +186,12 @@ __device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Barrier of the two warps that share a 32-token block: named barriers 3..10
+// (0 is __syncthreads, 1 and 2 the team barriers).
+__device__ __forceinline__ void pair_bar(int pair) {
+  asm volatile("bar.sync %0, 64;" ::"r"(3 + pair) : "memory");
+}
+
 // Exact path of a code: bits of fl(fl(x / s) + kMagic), whose low byte is
 // rint_even(fl(x / s)) as an int8. Out of line: the fast path below decides
 // all but a few codes in 10^4.
@@ -176,13 +199,15 @@ __device__ __noinline__ uint32_t exact_code_bits(float x, float s) {
   return __float_as_uint(__fadd_rn(__fdiv_rn(x, s), kMagic));
 }
 
-// INT8 codes and scale of one 32-token block: x (kMu false) or fl(x - mu)
-// (kMu true; nmu holds -mu for the lane's 8 channels as pairs). Reads the
-// warp's 32 rows of a shared tile with 8-channel lanes; writes rows
-// s0..s0+31 of f16_bh ([S_pad][128], the codes as fp16 values) and, when
-// codes_bh is not null, of codes_bh ([S_pad][128] int8), with streaming
-// stores; rows at or past nvalid are written as zero codes. kFull: nvalid is
-// 32. Returns the scale.
+// One warp's half (16 tokens) of a 32-token INT8 block: codes and scale of x
+// (kMu false) or of fl(x - mu) (kMu true; nmu holds -mu for the lane's 8
+// channels as pairs). rows: the warp's 16 rows of a shared tile, read with
+// 8-channel lanes; nvalid: how many of them are below S (kFull: all 16). The
+// block's amax is the max of both halves: each warp posts its own in
+// x_mine and reads the other's from x_other after the pair barrier. Writes
+// rows s0 .. s0+15 of f16_bh ([S_pad][128], the codes as fp16 values) and,
+// when codes_bh is not null, of codes_bh ([S_pad][128] int8), with streaming
+// stores; rows at or past nvalid get zero codes. Returns the scale.
 //
 // Fast path for the codes (two-element packed arithmetic): t = fl(x*r + M)
 // with r = fl(1/s) and M = 1.5*2^23 is M + rint_even(x*r) (the spacing of
@@ -190,15 +215,16 @@ __device__ __noinline__ uint32_t exact_code_bits(float x, float s) {
 // 2^-17 of x/s, and so is fl(x/s) (|x/s| <= 127.5), so when |g| < 1/2 - 2^-15
 // the code c is rint_even(fl(x/s)); otherwise the exact division decides.
 template <bool kMu, bool kFull>
-__device__ __forceinline__ float quantize_block(const uint8_t* rows, const float2 (&nmu)[4], int nvalid,
-                                                int8_t* codes_bh, uint16_t* f16_bh, int64_t s0, int lane) {
+__device__ __forceinline__ float quantize_half_block(const uint8_t* rows, const float2 (&nmu)[4], int nvalid,
+                                                     int8_t* codes_bh, uint16_t* f16_bh, int64_t s0, int lane,
+                                                     volatile float* x_mine, volatile float* x_other, int pair) {
   const int half = lane >> 4;
   float a;
   if (!kMu) {
-    // block amax on the bf16 bit patterns (magnitudes order as integers)
+    // amax on the bf16 bit patterns (magnitudes order as integers)
     uint32_t m0 = 0u, m1 = 0u;
-#pragma unroll 8
-    for (int i = 0; i < 16; ++i) {
+#pragma unroll
+    for (int i = 0; i < kHalfRows / 2; ++i) {
       const int t = 2 * i + half;
       if (kFull || t < nvalid) {
         const uint4 w = tok8(rows, t, lane);
@@ -210,8 +236,8 @@ __device__ __forceinline__ float quantize_block(const uint8_t* rows, const float
     a = __uint_as_float(warp_max_u32(max(m & 0xFFFFu, m >> 16)) << 16);
   } else {
     float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll 8
-    for (int i = 0; i < 16; ++i) {
+#pragma unroll
+    for (int i = 0; i < kHalfRows / 2; ++i) {
       const int t = 2 * i + half;
       if (kFull || t < nvalid) {
         const uint4 w = tok8(rows, t, lane);
@@ -225,6 +251,9 @@ __device__ __forceinline__ float quantize_block(const uint8_t* rows, const float
     }
     a = warp_max(fmaxf(a0, a1));
   }
+  if (lane == 0) *x_mine = a;
+  pair_bar(pair);
+  a = fmaxf(a, *x_other);
   const float s = __fdiv_rn(a, kInt8Max);
   const bool fast = s >= FLT_MIN;
   const float r = fast ? __frcp_rn(s) : 0.0f;
@@ -232,8 +261,9 @@ __device__ __forceinline__ float quantize_block(const uint8_t* rows, const float
   const float2 m2 = make_float2(kMagic, kMagic), nm2 = make_float2(-kMagic, -kMagic);
   uint2* out8 = codes_bh ? reinterpret_cast<uint2*>(codes_bh + s0 * kHeadDim) + (lane & 15) : nullptr;
   uint4* out16 = reinterpret_cast<uint4*>(f16_bh + s0 * kHeadDim) + (lane & 15);
-#pragma unroll 4
-  for (int i = 0; i < 16; ++i) {
+  uint32_t redo = 0u;  // bit i: row 2i + half needs the exact division
+#pragma unroll
+  for (int i = 0; i < kHalfRows / 2; ++i) {
     const int t = 2 * i + half;
     uint2 c8 = make_uint2(0u, 0u);
     uint4 c16 = make_uint4(0u, 0u, 0u, 0u);
@@ -253,23 +283,44 @@ __device__ __forceinline__ float quantize_block(const uint8_t* rows, const float
         const float2 gk = __ffma2_rn(x[k], nr2, cc[k]);
         g = max3(g, fabsf(gk.x), fabsf(gk.y));
       }
-      if (!(fast && g < kHalfGuard)) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          tt[k].x = __uint_as_float(exact_code_bits(x[k].x, s));
-          tt[k].y = __uint_as_float(exact_code_bits(x[k].y, s));
-          cc[k] = __fadd2_rn(tt[k], nm2);
-        }
-      }
-      c8.x = pack_low_bytes(__float_as_uint(tt[0].x), __float_as_uint(tt[0].y), __float_as_uint(tt[1].x),
-                            __float_as_uint(tt[1].y));
-      c8.y = pack_low_bytes(__float_as_uint(tt[2].x), __float_as_uint(tt[2].y), __float_as_uint(tt[3].x),
-                            __float_as_uint(tt[3].y));
+      if (!(fast && g < kHalfGuard)) redo |= 1u << i;
+      c8 = make_uint2(pack_low_bytes(__float_as_uint(tt[0].x), __float_as_uint(tt[0].y), __float_as_uint(tt[1].x),
+                                     __float_as_uint(tt[1].y)),
+                      pack_low_bytes(__float_as_uint(tt[2].x), __float_as_uint(tt[2].y), __float_as_uint(tt[3].x),
+                                     __float_as_uint(tt[3].y)));
       c16 = make_uint4(f16x2(cc[0].x, cc[0].y), f16x2(cc[1].x, cc[1].y), f16x2(cc[2].x, cc[2].y),
                        f16x2(cc[3].x, cc[3].y));
     }
     if (out8) __stcs(out8 + t * (kHeadDim / 8), c8);
     __stcs(out16 + t * (kHeadDim / 8), c16);
+  }
+  if (redo != 0u) {
+    // rare: rows where a fast code could be off by one are recomputed by the
+    // exact division and stored again (same thread, same address: the later
+    // store wins)
+#pragma unroll 1
+    for (int i = 0; i < kHalfRows / 2; ++i) {
+      if (!((redo >> i) & 1u)) continue;
+      const int t = 2 * i + half;
+      const uint4 w = tok8(rows, t, lane);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      uint32_t b[8];
+      float cf[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float2 x = bf2(ws[k]);
+        if (kMu) x = __fadd2_rn(x, nmu[k]);
+        b[2 * k] = exact_code_bits(x.x, s);
+        b[2 * k + 1] = exact_code_bits(x.y, s);
+        cf[2 * k] = __fsub_rn(__uint_as_float(b[2 * k]), kMagic);
+        cf[2 * k + 1] = __fsub_rn(__uint_as_float(b[2 * k + 1]), kMagic);
+      }
+      if (out8)
+        __stcs(out8 + t * (kHeadDim / 8),
+               make_uint2(pack_low_bytes(b[0], b[1], b[2], b[3]), pack_low_bytes(b[4], b[5], b[6], b[7])));
+      __stcs(out16 + t * (kHeadDim / 8),
+             make_uint4(f16x2(cf[0], cf[1]), f16x2(cf[2], cf[3]), f16x2(cf[4], cf[5]), f16x2(cf[6], cf[7])));
+    }
   }
   return s;
 }
@@ -286,33 +337,46 @@ __device__ __noinline__ double fp64_chunk_sum(const uint8_t* rows, int nvalid, i
   return p;
 }
 
-// Exact fp64 sums of one 32-token chunk for the lane's 8 channels (8-channel
-// lanes; results valid in every lane, for channels 8*(lane & 15) .. +8).
-//
-// Each half-warp runs one float-pair chain per channel over its 16 tokens
-// (TwoSum: hi + lo stays the exact running sum while lo's own additions are
-// exact); the two chains are joined across the half-warps with one more
-// TwoSum. Exactness: every input is a multiple of 2^L, L the last-bit weight
-// of the smallest nonzero magnitude in the lane's channels; with E the
-// exponent of the largest magnitude, every partial sum is below 32 * 2^(E+1)
-// = 2^(E+6) in magnitude, so every TwoSum error is a multiple of 2^L below
-// 2^(E-19), and lo, which adds 33 of them, stays below 2^(E-13). lo's sums
-// are therefore exact in fp32 while E - 13 <= L + 24; the code takes the fast
-// result when E - L <= 36. The exact total T = hi + lo is then a multiple of
-// 2^L below 2^(E+6) and fits in 53 bits, as does every prefix of the
-// left-to-right fp64 sum, which is therefore exact too and equals T;
-// fl64(hi + lo) = T. Otherwise the chunk is summed left to right in fp64.
-template <bool kFull>
-__device__ __forceinline__ void chunk_sums(const uint8_t* rows, int nvalid, int lane, double (&out)[8]) {
-  const int half = lane >> 4;
+// TwoSum of pairs: s = fl(a + b) and the exact error e = (a + b) - s.
+__device__ __forceinline__ void two_sum2(float2 a, float2 b, float2& s, float2& e) {
   const float2 neg1 = make_float2(-1.0f, -1.0f);
-  float2 hi[4], lo[4];
+  s = __fadd2_rn(a, b);
+  const float2 bb = __ffma2_rn(a, neg1, s);                       // s - a
+  const float2 ea = __ffma2_rn(__ffma2_rn(bb, neg1, s), neg1, a);  // a - (s - bb)
+  const float2 eb = __ffma2_rn(bb, neg1, b);                       // b - bb
+  e = __fadd2_rn(ea, eb);
+}
+
+// One warp's part of the exact fp64 sums of a 32-token key chunk: its 16
+// rows (8-channel lanes), summed by one float-pair chain per channel in each
+// half-warp and joined across the half-warps. On return every lane holds, for
+// channels 8*(lane & 15) .. +8 as pairs, hi + lo = the exact sum of its rows
+// (while lo's additions are exact, see below), and mx / mn the largest
+// magnitude bits and (smallest nonzero magnitude bits - 1) of its rows, per
+// 16-bit half.
+//
+// Exactness (the two warps of a chunk are joined the same way by the
+// caller): every input is a multiple of 2^L, L the last-bit weight of the
+// smallest nonzero magnitude among the chunk's values in these channels; with
+// E the exponent of the largest magnitude, every partial sum is below
+// 32 * 2^(E+1) = 2^(E+6), so every TwoSum error is a multiple of 2^L below
+// 2^(E-19), and lo, which adds 35 of them (four chains of 8 tokens and three
+// joins), stays below 2^(E-13). lo's sums are therefore exact in fp32 while
+// E - 13 <= L + 24; the fast result is used when E - L <= 36. The exact total
+// T = hi + lo is then a multiple of 2^L below 2^(E+6) and fits in 53 bits, as
+// does every prefix of the left-to-right fp64 sum, which is therefore exact
+// too and equals T; fl64(hi + lo) = T. Otherwise the chunk is summed left to
+// right in fp64.
+template <bool kFull>
+__device__ __forceinline__ void key_sum_partial(const uint8_t* rows, int nvalid, int lane, float2 (&hi)[4],
+                                                float2 (&lo)[4], uint32_t& mx, uint32_t& mn) {
+  const int half = lane >> 4;
 #pragma unroll
   for (int k = 0; k < 4; ++k) hi[k] = lo[k] = make_float2(0.0f, 0.0f);
-  uint32_t mx0 = 0u, mx1 = 0u;                 // largest magnitude bits, per 16-bit half
-  uint32_t mn0 = 0xFFFFFFFFu, mn1 = 0xFFFFFFFFu;  // (magnitude bits - 1); zeros wrap to 0xFFFF
+  uint32_t mx0 = 0u, mx1 = 0u;
+  uint32_t mn0 = 0xFFFFFFFFu, mn1 = 0xFFFFFFFFu;  // zeros wrap to 0xFFFF and never win
 #pragma unroll 4
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < kHalfRows / 2; ++i) {
     const int t = 2 * i + half;
     if (kFull || t < nvalid) {
       const uint4 w = tok8(rows, t, lane);
@@ -324,43 +388,41 @@ __device__ __forceinline__ void chunk_sums(const uint8_t* rows, int nvalid, int 
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float2 x = bf2(ws[k]);
-        const float2 sum = __fadd2_rn(hi[k], x);
-        const float2 bb = __ffma2_rn(hi[k], neg1, sum);                       // sum - hi
-        const float2 t2 = __ffma2_rn(__ffma2_rn(bb, neg1, sum), neg1, hi[k]);  // hi - (sum - bb)
-        const float2 t3 = __ffma2_rn(bb, neg1, x);                             // x - bb
-        hi[k] = sum;
-        lo[k] = __fadd2_rn(lo[k], __fadd2_rn(t2, t3));
+        float2 s, e;
+        two_sum2(hi[k], bf2(ws[k]), s, e);
+        hi[k] = s;
+        lo[k] = __fadd2_rn(lo[k], e);
       }
     }
   }
-  // join the two half-warps' chains (both halves compute the same result)
-  uint32_t mx = __vmaxu2(mx0, mx1), mn = __vminu2(mn0, mn1);
-  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-  mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
-  const uint32_t mxb = max(mx & 0xFFFFu, mx >> 16);
-  const uint32_t mnb = min(mn & 0xFFFFu, mn >> 16) + 1u;  // 0x10000 when every value is zero
-  int ef_min = static_cast<int>((mnb >> 7) & 0xFFu);
-  if (ef_min == 0) ef_min = 1;  // subnormal bf16: last-bit weight 2^-133
-  int ef_max = static_cast<int>(mxb >> 7);
-  if (ef_max == 0) ef_max = 1;
-  const bool exact = mnb > 0x7FFFu || ef_max - ef_min <= 36 - 7;  // E - L = (ef_max - ef_min) + 7
+  mx = __vmaxu2(mx0, mx1);
+  mn = __vminu2(mn0, mn1);
+  mx = __vmaxu2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  mn = __vminu2(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
+  // join the half-warps' chains (both halves compute the same result)
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const float2 ohi = make_float2(__shfl_xor_sync(0xffffffffu, hi[k].x, 16), __shfl_xor_sync(0xffffffffu, hi[k].y, 16));
     const float2 olo = make_float2(__shfl_xor_sync(0xffffffffu, lo[k].x, 16), __shfl_xor_sync(0xffffffffu, lo[k].y, 16));
-    const float2 sum = __fadd2_rn(hi[k], ohi);
-    const float2 bb = __ffma2_rn(hi[k], neg1, sum);
-    const float2 t2 = __ffma2_rn(__ffma2_rn(bb, neg1, sum), neg1, hi[k]);
-    const float2 t3 = __ffma2_rn(bb, neg1, ohi);
-    const float2 l = __fadd2_rn(__fadd2_rn(lo[k], olo), __fadd2_rn(t2, t3));
-    out[2 * k] = __dadd_rn(static_cast<double>(sum.x), static_cast<double>(l.x));
-    out[2 * k + 1] = __dadd_rn(static_cast<double>(sum.y), static_cast<double>(l.y));
+    float2 s, e;
+    two_sum2(hi[k], ohi, s, e);
+    hi[k] = s;
+    lo[k] = __fadd2_rn(__fadd2_rn(lo[k], olo), e);
   }
-  if (!exact) {
-#pragma unroll 1
-    for (int c = 0; c < 8; ++c) out[c] = fp64_chunk_sum(rows, nvalid, (lane & 15) * 16 + 2 * c);
-  }
+}
+
+// True when the float-pair chunk sums are exact (see key_sum_partial), from
+// the chunk's largest magnitude bits and (smallest nonzero magnitude bits - 1)
+// per 16-bit half.
+__device__ __forceinline__ bool key_sum_exact(uint32_t mx, uint32_t mn) {
+  const uint32_t mxb = max(mx & 0xFFFFu, mx >> 16);
+  const uint32_t mnb = min(mn & 0xFFFFu, mn >> 16) + 1u;  // 0x10000 when every value is zero
+  if (mnb > 0x7FFFu) return true;
+  int ef_min = static_cast<int>(mnb >> 7);
+  if (ef_min == 0) ef_min = 1;  // subnormal bf16: last-bit weight 2^-133
+  int ef_max = static_cast<int>(mxb >> 7);
+  if (ef_max == 0) ef_max = 1;
+  return ef_max - ef_min <= 36 - 7;  // E - L = (ef_max - 127) - (ef_min - 134)
 }
 
 // Two e4m3 codes: high byte = code(a), low byte = code(b).
@@ -377,29 +439,45 @@ __device__ __noinline__ uint32_t exact_v_quad(uint2 w, float4 s) {
   return p01 | (p23 << 16);
 }
 
-// V codes of one token's 4 channels (4-channel lanes), low byte = channel 0.
-// Rounding to e4m3 is monotone, and fl(v / s) lies within 2^-22 relative of
+// Fast V codes of one token's 4 channels (4-channel lanes), low byte =
+// channel 0; returns false when the exact division must decide. Rounding to
+// e4m3 is monotone, and fl(v / s) lies within 2^-22 relative of
 // q = fl(v * fl(1/s)); so when q * (1 - 2^-21) and q * (1 + 2^-21) round to
-// the same code, that is the code of fl(v / s); otherwise the exact division
-// decides.
-__device__ __forceinline__ uint32_t v_code_quad(uint2 w, float2 r01, float2 r23, float4 s, bool fast) {
+// the same code, that is the code of fl(v / s).
+__device__ __forceinline__ bool v_code_quad_fast(uint2 w, float2 r01, float2 r23, uint32_t& code) {
   const float2 q01 = __fmul2_rn(bf2(w.x), r01), q23 = __fmul2_rn(bf2(w.y), r23);
   const float2 dn = make_float2(kDn, kDn), up = make_float2(kUp, kUp);
   const float2 d01 = __fmul2_rn(q01, dn), u01 = __fmul2_rn(q01, up);
   const float2 d23 = __fmul2_rn(q23, dn), u23 = __fmul2_rn(q23, up);
   const uint32_t cd = e4m3x2(d01.y, d01.x) | (e4m3x2(d23.y, d23.x) << 16);
   const uint32_t cu = e4m3x2(u01.y, u01.x) | (e4m3x2(u23.y, u23.x) << 16);
-  if (fast && cd == cu) return cd;
-  return exact_v_quad(w, s);
+  code = cd;
+  return cd == cu;
 }
 
 // Pairwise tree (padded with +0.0 to a power of two) over `n` group sums
 // starting at p, stride 128 doubles, evaluated streaming: stack[l] holds a
-// finished subtree of 2^l leaves. The sums are never -0.0, so padding with
-// +0.0 changes nothing.
+// finished subtree of 2^l leaves. Aligned blocks of 16 leaves are loaded
+// together (16 loads in flight) and reduced as one 16-leaf subtree, which is
+// what pushing the 16 leaves one by one would build. The sums are never
+// -0.0, so padding with +0.0 changes nothing.
 __device__ __forceinline__ double tree_sum(const double* p, int64_t n) {
   double stack[40];
-  for (int64_t gi = 0; gi < n; ++gi) {
+  int64_t gi = 0;
+  for (; gi + 16 <= n; gi += 16) {
+    double v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = __ldcg(p + (gi + k) * kHeadDim);
+#pragma unroll
+    for (int w = 1; w < 16; w *= 2)
+#pragma unroll
+      for (int k = 0; k < 16; k += 2 * w) v[k] = __dadd_rn(v[k], v[k + w]);
+    double val = v[0];
+    int lvl = 4;
+    for (int64_t k = gi >> 4; k & 1; k >>= 1, ++lvl) val = __dadd_rn(stack[lvl], val);
+    stack[lvl] = val;
+  }
+  for (; gi < n; ++gi) {
     double val = __ldcg(p + gi * kHeadDim);
     int lvl = 0;
     for (int64_t k = gi; k & 1; k >>= 1, ++lvl) val = __dadd_rn(stack[lvl], val);
@@ -416,8 +494,25 @@ __device__ __forceinline__ double tree_sum(const double* p, int64_t n) {
   return carry;
 }
 
+// Max of `n` group maxima starting at p, stride 128 floats, 16 loads in flight.
+__device__ __forceinline__ float group_max(const float* p, int64_t n) {
+  float m = 0.0f;
+  int64_t gi = 0;
+  for (; gi + 16 <= n; gi += 16) {
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = __ldcg(p + (gi + k) * kHeadDim);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) m = fmaxf(m, v[k]);
+  }
+  for (; gi < n; ++gi) m = fmaxf(m, __ldcg(p + gi * kHeadDim));
+  return m;
+}
+
 // Barrier of one compute team (named barrier 1 + team, 256 threads).
-__device__ __forceinline__ void team_bar(int team) { asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "n"(kGroup) : "memory"); }
+__device__ __forceinline__ void team_bar(int team) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "n"(kTeamThreads) : "memory");
+}
 
 struct Ctx {
   uint32_t bar0;
@@ -425,6 +520,8 @@ struct Ctx {
   int* dev_err;
   __device__ uint32_t full(int s) const { return bar0 + 8u * static_cast<uint32_t>(s); }
   __device__ uint32_t empty(int s) const { return bar0 + 8u * static_cast<uint32_t>(kStages + s); }
+  __device__ uint32_t evt_full(int e) const { return bar0 + 8u * static_cast<uint32_t>(2 * kStages + e); }
+  __device__ uint32_t evt_empty(int e) const { return bar0 + 8u * static_cast<uint32_t>(2 * kStages + kEvents + e); }
 };
 
 // Bounded wait on an mbarrier phase; on expiry sets the error word and the
@@ -448,25 +545,43 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint32_t bar, uint32_t p
   }
 }
 
-// Bounded wait until ready[bh] is set by the CTA that finished the head.
-__device__ __forceinline__ bool wait_ready(const Ctx& cx, const unsigned* flag) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (v != 0u) return true;
-    __nanosleep(64);
-    if ((it & 63u) == 63u) {
-      if (*cx.abort_flag) return false;
-      const uint64_t now = tc::global_timer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > kTimeoutNs) {
-        *cx.abort_flag = 1;
-        atomicExch(cx.dev_err, kDevErrTimeout);
-        return false;
-      }
+
+// Finish head bh with the 256 threads of team 1: the pairwise tree over its
+// group key sums gives the key mean, the max over its group maxima the V
+// scales; then the head is published as ready. Every group of the head has
+// been counted (by the producer of this CTA, which saw the count complete).
+__device__ __forceinline__ void finish_head(const Params& prm, int64_t bh, int tt, double* fin_right,
+                                            float* fin_vmax) {
+  const int64_t G = prm.G;
+  const int c = tt & (kHeadDim - 1), hf = tt >> 7;
+  int64_t P = 1;
+  while (P < G) P *= 2;
+  const int64_t lo = hf == 0 ? 0 : (P == 1 ? 1 : P / 2);
+  const int64_t hi_end = hf == 0 ? (P == 1 ? 1 : P / 2) : P;
+  const int64_t n = max(int64_t(0), min(G, hi_end) - lo);
+  double t = 0.0;
+  if (prm.smooth_k && n > 0) t = tree_sum(prm.ksum + (bh * G + lo) * kHeadDim + c, n);
+  const float vmx = n > 0 ? group_max(prm.vmax + (bh * G + lo) * kHeadDim + c, n) : 0.0f;
+  if (hf == 1) {
+    fin_right[c] = t;
+    fin_vmax[c] = vmx;
+  }
+  team_bar(1);
+  if (hf == 0) {
+    float mu = 0.0f;
+    if (prm.smooth_k) {
+      const double total = P > 1 ? __dadd_rn(t, fin_right[c]) : t;
+      mu = __double2float_rn(__ddiv_rn(total, static_cast<double>(prm.S)));
     }
+    prm.out.k_mean[bh * kHeadDim + c] = mu;
+    prm.out.v_scale[bh * kHeadDim + c] = __fdiv_rn(fmaxf(vmx, fin_vmax[c]), kE4M3Max);
+  }
+  team_bar(1);
+  if (tt == 0) {
+    // release: the mean and scales written by the team (ordered by the
+    // barrier) are visible to whoever acquires the flag
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(prm.ready + bh), "r"(1u) : "memory");
   }
 }
 
@@ -475,82 +590,214 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const Params prm, int3 s_axis) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ double ks[kWarps][kHeadDim];
-  __shared__ uint32_t vm[kWarps][kHeadDim / 2];
+  __shared__ double ks[kChunks][kHeadDim];            // exact chunk sums of the current group
+  __shared__ uint32_t vm[kWarps][kHeadDim / 2];       // per-warp max |v| bits, channel pairs
+  __shared__ float xk_hi[kChunks][kHeadDim], xk_lo[kChunks][kHeadDim];  // second-half key sums
+  __shared__ uint32_t xk_bits[kChunks][2];            // second-half magnitude bounds
+  __shared__ float xa[2][kTeams * kWarps / 2][2];     // amax of each half block, two parities
   __shared__ float fin_vmax[kHeadDim];
   __shared__ double fin_right[kHeadDim];
-  __shared__ int last_flag;  // stats items: this CTA finished the head
   const uint32_t sbase = tc::smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t* meta_item = reinterpret_cast<int64_t*>(smem + kOffMeta);             // [kStages]
   int* meta_tensor = reinterpret_cast<int*>(smem + kOffMeta + kStages * 8);     // [kStages]
+  volatile int64_t* evt_bh = reinterpret_cast<volatile int64_t*>(smem + kOffEvt);  // [kEvents]
+  int64_t* fin_q = reinterpret_cast<int64_t*>(smem + kOffFinQ);                 // [kFinCap]
+  const float* hstat = reinterpret_cast<const float*>(smem + kOffHstat);        // [kStages][256]
   Ctx cx;
   cx.bar0 = sbase + kOffBar;
   cx.abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlags);
   cx.dev_err = prm.dev_err;
   if (threadIdx.x == 0) {
     *cx.abort_flag = 0;
+    *reinterpret_cast<volatile uint32_t*>(smem + kOffFlags + 4) = 0u;  // finish-queue tail
+    *reinterpret_cast<volatile uint32_t*>(smem + kOffFlags + 8) = 0u;  // groups counted
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(cx.full(s), 1);
-      tc::mbar_init(cx.empty(s), kTeams * kGroup);  // both teams release every stage
+      tc::mbar_init(cx.empty(s), kTeams * kTeamThreads);  // both teams release every stage
+    }
+    for (int e = 0; e < kEvents; ++e) {
+      tc::mbar_init(cx.evt_full(e), 1);
+      tc::mbar_init(cx.evt_empty(e), 1);
     }
     tc::fence_mbar_init();
   }
   __syncthreads();
 
+  volatile uint32_t* fin_tail_p = reinterpret_cast<volatile uint32_t*>(smem + kOffFlags + 4);  // finish queue tail
+  volatile uint32_t* counted_p = reinterpret_cast<volatile uint32_t*>(smem + kOffFlags + 8);   // groups counted
+
+  if (warp == kTeams * kWarps + 1) {
+    // --------------------------------------------------------------- counter --
+    // Counts the groups team 1 reports done. The fence and atomic of the count
+    // stay off the compute warps and off the producer (a fence there would
+    // also wait for its tile loads). When a head's last group is counted the
+    // head goes into the finish queue; the producer turns it into a finish
+    // marker for team 1. A report with head -1 ends the loop.
+    if (lane == 0) {
+      uint32_t ev = 0, tail = 0;
+      while (true) {
+        const uint32_t e = ev % kEvents;
+        if (!wait_bar(cx, cx.evt_full(e), (ev / kEvents) & 1u)) break;
+        const int64_t h = evt_bh[e];
+        tc::mbar_arrive(cx.evt_empty(e));
+        ++ev;
+        if (h < 0) break;
+        // team 1's slot writes are ordered before the report (barrier, then
+        // release on the mbarrier); the fence makes them visible to the GPU
+        // before the count
+        __threadfence();
+        if (atomicAdd(prm.done + h, 1u) == static_cast<unsigned>(prm.G - 1)) {
+          __threadfence();  // acquire the other CTAs' group results
+          // the queue never holds more than the groups in flight in this CTA
+          // (tiles in the ring plus reports), far below its capacity
+          fin_q[tail % kFinCap] = h;
+          __threadfence_block();
+          *fin_tail_p = ++tail;
+        }
+        __threadfence_block();
+        *counted_p = ev;
+      }
+    }
+    return;
+  }
+
   if (warp == kTeams * kWarps) {
     // -------------------------------------------------------------- producer --
+    // Claims items in order and loads their tiles into the ring. Heads the
+    // counter warp has finished counting become finish markers, pushed at
+    // item boundaries (between the tiles of an item the consumers expect no
+    // marker); the codes items of a head enter the ring only after team 1
+    // has finished and published it.
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_k);
       tc::prefetch_tmap(&tm_v);
-      uint32_t cnt = 0;
-      int pending[kStages] = {-1, -1, -1};
+      // Q is read once; K and V are read by the stats item and again by the
+      // codes item lag heads later, so they are kept in L2 until then
+      const uint64_t pol_first = tc::policy_evict_first(), pol_last = tc::policy_evict_last();
+      uint32_t cnt = 0, stats_pushed = 0, fin_head = 0;
+      int pending[kStages];
+      for (int s = 0; s < kStages; ++s) pending[s] = -1;
       bool ok = true;
-      while (ok) {
-        const int64_t item = static_cast<int64_t>(atomicAdd(prm.next_item, 1u));
-        const bool end = item >= prm.total;
-        int tensors[3], nt = 0;
-        Item it{0, 0, 0};
-        if (end) {
-          tensors[nt++] = kEnd;
-        } else {
-          it = decode_item(item, prm.NH, prm.G, prm.lag);
-          if (it.phase == 0) {
-            tensors[nt++] = kTensorQ;
-            if (prm.smooth_k) tensors[nt++] = kTensorK;
-            tensors[nt++] = kTensorV;
-          } else {
-            // a codes item needs the head's key mean and V scales: its tiles
-            // enter the ring only once they are published
-            if (!(ok = wait_ready(cx, prm.ready + it.bh))) break;
-            tensors[nt++] = kTensorK;
-            tensors[nt++] = kTensorV;
+      auto fins_waiting = [&]() { return *fin_tail_p != fin_head; };
+      // push one finish marker into stage st (the stage is free)
+      auto push_finish = [&](uint32_t st) {
+        __threadfence_block();  // the queue entry after its tail
+        meta_item[st] = fin_q[fin_head++ % kFinCap];
+        meta_tensor[st] = kFinish;
+        tc::mbar_arrive(cx.full(st));
+        ++cnt;
+      };
+      // queued finish markers go into free stages without waiting
+      auto push_finish_markers = [&]() {
+        while (fins_waiting() && tc::mbar_try_wait(cx.empty(cnt % kStages), ((cnt / kStages) & 1u) ^ 1u))
+          push_finish(cnt % kStages);
+      };
+      // the next ring position, once both teams have released it
+      auto next_stage = [&](uint32_t& st, uint32_t& ph) -> bool {
+        st = cnt % kStages;
+        ph = (cnt / kStages) & 1u;
+        return wait_bar(cx, cx.empty(st), ph ^ 1u);
+      };
+      // bounded wait for a condition
+      auto wait_until = [&](auto cond) -> bool {
+        uint64_t t0 = 0;
+        for (uint32_t it = 0;; ++it) {
+          if (cond()) return true;
+          if ((it & 63u) == 63u) {
+            if (*cx.abort_flag) return false;
+            const uint64_t now = tc::global_timer_ns();
+            if (t0 == 0) {
+              t0 = now;
+            } else if (now - t0 > kTimeoutNs) {
+              *cx.abort_flag = 1;
+              atomicExch(cx.dev_err, kDevErrTimeout);
+              return false;
+            }
+            __nanosleep(32);
           }
         }
-        for (int n = 0; n < nt && ok; ++n) {
-          const uint32_t st = cnt % kStages, ph = (cnt / kStages) & 1u;
-          if (!(ok = wait_bar(cx, cx.empty(st), ph ^ 1u))) break;
-          meta_item[st] = end ? -1 : item;
-          meta_tensor[st] = tensors[n];
-          if (tensors[n] == kEnd) {
+      };
+      // the next claim is issued one item ahead so its latency overlaps the
+      // waits for free stages (items are still processed in claim order)
+      unsigned next = atomicAdd(prm.next_item, 1u);
+      bool claimed_end = false;
+      while (ok) {
+        uint32_t st, ph;
+        if (fins_waiting()) {
+          if (!(ok = next_stage(st, ph))) break;
+          push_finish(st);
+          continue;
+        }
+        if (claimed_end) {
+          // every stats item pushed is counted, and its head finished if it
+          // was the last group, before the end marker
+          if (*counted_p == stats_pushed) {
+            if (fins_waiting()) continue;
+            if (!(ok = next_stage(st, ph))) break;
+            meta_item[st] = -1;
+            meta_tensor[st] = kEnd;
             tc::mbar_arrive(cx.full(st));
-          } else {
-            tc::mbar_arrive_expect_tx(cx.full(st), kTileBytes);
-            const CUtensorMap* tm = tensors[n] == kTensorQ ? &tm_q : (tensors[n] == kTensorK ? &tm_k : &tm_v);
-            const int32_t h = static_cast<int32_t>(it.bh % prm.H), b = static_cast<int32_t>(it.bh / prm.H);
-            const int32_t s0 = static_cast<int32_t>(it.g * kGroup);
-            // map dims: (channel, s, h, b) or (channel, h, s, b) by stride order
-            const int ax = tensors[n] == kTensorQ ? s_axis.x : (tensors[n] == kTensorK ? s_axis.y : s_axis.z);
-            if (ax == 1)
-              tc::tma_load_4d(sbase + st * kTileBytes, tm, 0, s0, h, b, cx.full(st));
-            else
-              tc::tma_load_4d(sbase + st * kTileBytes, tm, 0, h, s0, b, cx.full(st));
-            pending[st] = static_cast<int>(ph);
+            break;
           }
+          ok = wait_until([&] { return *counted_p == stats_pushed || fins_waiting(); });
+          continue;
+        }
+        const int64_t item = static_cast<int64_t>(next);
+        if (item >= prm.total) {
+          claimed_end = true;
+          continue;
+        }
+        next = atomicAdd(prm.next_item, 1u);
+        const Item it = decode_item(item, prm.NH, prm.G, prm.lag);
+        int tensors[3], nt = 0;
+        if (it.phase == 0) {
+          tensors[nt++] = kTensorQ;
+          if (prm.smooth_k) tensors[nt++] = kTensorK;
+          tensors[nt++] = kTensorV;
+        } else {
+          // a codes item needs the head's key mean and V scales: its tiles
+          // enter the ring only once they are published. Meanwhile queued
+          // finish markers must still reach team 1 (the head waited for may
+          // be one of them)
+          const unsigned* flag = prm.ready + it.bh;
+          if (!(ok = wait_until([&] {
+                  push_finish_markers();
+                  unsigned v;
+                  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+                  return v != 0u;
+                })))
+            break;
+          tc::fence_proxy_async_global();  // the bulk copies below read what the flag published
+          tensors[nt++] = kTensorK;
+          tensors[nt++] = kTensorV;
+        }
+        const int32_t h = static_cast<int32_t>(it.bh % prm.H), b = static_cast<int32_t>(it.bh / prm.H);
+        const int32_t s0 = static_cast<int32_t>(it.g * kItemTokens);
+        for (int n = 0; n < nt && ok; ++n) {
+          if (!(ok = next_stage(st, ph))) break;
+          meta_item[st] = item;
+          meta_tensor[st] = tensors[n];
+          const bool with_stats = it.phase == 1 && n == 0;  // the codes item's head statistics
+          tc::mbar_arrive_expect_tx(cx.full(st), kTileBytes + (with_stats ? kHstatBytes : 0u));
+          const CUtensorMap* tm = tensors[n] == kTensorQ ? &tm_q : (tensors[n] == kTensorK ? &tm_k : &tm_v);
+          // map dims: (channel, s, h, b) or (channel, h, s, b) by stride order
+          const int ax = tensors[n] == kTensorQ ? s_axis.x : (tensors[n] == kTensorK ? s_axis.y : s_axis.z);
+          const uint64_t pol = (it.phase == 0 && tensors[n] != kTensorQ) ? pol_last : pol_first;
+          if (ax == 1)
+            tc::tma_load_4d_hint(sbase + st * kTileBytes, tm, 0, s0, h, b, cx.full(st), pol);
+          else
+            tc::tma_load_4d_hint(sbase + st * kTileBytes, tm, 0, h, s0, b, cx.full(st), pol);
+          if (with_stats) {
+            const uint32_t hs = sbase + kOffHstat + st * kHstatBytes;
+            tc::bulk_load(hs, prm.out.k_mean + it.bh * kHeadDim, kHeadDim * 4, cx.full(st));
+            tc::bulk_load(hs + kHeadDim * 4, prm.out.v_scale + it.bh * kHeadDim, kHeadDim * 4, cx.full(st));
+          }
+          pending[st] = static_cast<int>(ph);
           ++cnt;
         }
-        if (end) break;
+        if (ok && it.phase == 0) ++stats_pushed;
       }
       if (!ok) {
         Ctx drain = cx;
@@ -564,78 +811,138 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // --------------------------------------------------------------- compute --
-  // Two teams of 8 warps work on different tiles of the same item: team 0 on
-  // the first tile (Q of a stats item, K of a codes item), team 1 on the rest
-  // (K sums and V maxima of a stats item, V codes of a codes item). Both
+  // Two teams of 8 warps work on different tiles of the same item. Stats
+  // item: team 0 the Q tile; team 1 the K sums, the V maxima and the group's
+  // results. Codes item: team 1 the K tile, team 0 the V tile. Warps 2c and
+  // 2c+1 of a team take the two halves (16 tokens each) of chunk c. Both
   // teams wait on every stage in ring order, so a parity wait never meets a
   // barrier two phases behind; a team releases the stages it does not use as
   // soon as they are full, and a stage is refilled once both have released it.
-  // The tiles of a codes item enter the ring only after the producer has seen
-  // the head's statistics published, so the compute warps never wait for them.
-  const int team = warp / kWarps, tw = warp % kWarps, tt = threadIdx.x % kGroup;
+  const int team = warp / kWarps, tw = warp % kWarps, tt = threadIdx.x % kTeamThreads;
+  const int chunk = tw >> 1, sub = tw & 1, pair = warp >> 1;
   const int64_t S = prm.S, S_pad = prm.S_pad, G = prm.G;
-  uint32_t cnt = 0;
+  const int64_t nblk = S_pad / kQKBlock;
+  const uint32_t row_off = static_cast<uint32_t>(tw * kHalfRows * 256);
+  uint32_t cnt = 0, ev_cnt = 0;
+  int xpar = 0;  // slot parity of the amax exchange (both warps of a pair flip together)
   // wait for ring position c to be full, then release it unused
   auto pass = [&](uint32_t c) -> bool {
     if (!wait_bar(cx, cx.full(c % kStages), (c / kStages) & 1u)) return false;
     tc::mbar_arrive(cx.empty(c % kStages));
     return true;
   };
+  auto stage_rows = [&](uint32_t c) { return smem + (c % kStages) * kTileBytes + row_off; };
   while (true) {
     const uint32_t st = cnt % kStages;
     if (!wait_bar(cx, cx.full(st), (cnt / kStages) & 1u)) break;
     const int64_t item = meta_item[st];
-    if (meta_tensor[st] == kEnd) break;
+    const int tensor = meta_tensor[st];
+    if (tensor == kEnd) {
+      if (team == 1 && tt == 0) {
+        // tell the counter warp that no report follows
+        const uint32_t e = ev_cnt % kEvents;
+        if (wait_bar(cx, cx.evt_empty(e), ((ev_cnt / kEvents) & 1u) ^ 1u)) {
+          evt_bh[e] = -1;
+          tc::mbar_arrive(cx.evt_full(e));
+        }
+      }
+      break;
+    }
+    if (tensor == kFinish) {
+      tc::mbar_arrive(cx.empty(st));  // the marker carries no data
+      if (team == 1) finish_head(prm, item, tt, fin_right, fin_vmax);
+      cnt += 1;
+      continue;
+    }
     const Item it = decode_item(item, prm.NH, G, prm.lag);
     const uint32_t n_stages = it.phase == 0 ? (prm.smooth_k ? 3u : 2u) : 2u;
     const int64_t bh = it.bh;
-    const int64_t s0 = it.g * kGroup + tw * 32;
-    const int nvalid = valid_in_chunk(S, s0);
-    const bool in_pad = s0 < S_pad;  // rows past S_pad do not exist in the outputs
-    if (team == 1) tc::mbar_arrive(cx.empty(st));  // the first tile is team 0's
-    const uint32_t mine = cnt + static_cast<uint32_t>(team);  // this team's first ring position
-    const uint8_t* rows = smem + (mine % kStages) * kTileBytes + tw * 32 * 256;
+    const int64_t s0c = it.g * kItemTokens + chunk * kQKBlock;  // first token of the chunk
+    const int64_t s0 = s0c + sub * kHalfRows;                    // first token of this warp
+    const int nv = valid_rows(S, s0, kHalfRows);  // this warp's rows below S (every row is below S_pad)
+    volatile float* xm = &xa[xpar][pair][sub];
+    volatile float* xo = &xa[xpar][pair][sub ^ 1];
     bool ok = true;
 
-    if (team == 0 && it.phase == 0) {
+    if (it.phase == 0 && team == 0) {
       // Q codes and scale
-      if (in_pad) {
-        const float2 nz[4] = {};
-        int8_t* qc = prm.write_int8 ? prm.out.q_codes + bh * S_pad * kHeadDim : nullptr;
-        uint16_t* q16 = prm.out.q16 + bh * S_pad * kHeadDim;
-        const float s = nvalid == 32 ? quantize_block<false, true>(rows, nz, 32, qc, q16, s0, lane)
-                                     : quantize_block<false, false>(rows, nz, nvalid, qc, q16, s0, lane);
-        if (lane == 0) prm.out.q_scale[bh * (S_pad / kQKBlock) + s0 / kQKBlock] = s;
-      }
+      const float2 nz[4] = {};
+      int8_t* qc = prm.write_int8 ? prm.out.q_codes + bh * S_pad * kHeadDim : nullptr;
+      uint16_t* q16 = prm.out.q16 + bh * S_pad * kHeadDim;
+      const uint8_t* rows = stage_rows(cnt);
+      const float s = nv == kHalfRows
+                          ? quantize_half_block<false, true>(rows, nz, kHalfRows, qc, q16, s0, lane, xm, xo, pair)
+                          : quantize_half_block<false, false>(rows, nz, nv, qc, q16, s0, lane, xm, xo, pair);
+      xpar ^= 1;
+      if (sub == 0 && lane == 0) prm.out.q_scale[bh * nblk + s0c / kQKBlock] = s;
       tc::mbar_arrive(cx.empty(st));
       for (uint32_t c = 1; c < n_stages && ok; ++c) ok = pass(cnt + c);
       if (!ok) break;
-    } else if (team == 1 && it.phase == 0) {
-      // K tile: exact fp64 chunk sums
-      uint32_t c2 = mine;
+    } else if (it.phase == 0) {
+      tc::mbar_arrive(cx.empty(st));  // the Q tile is team 0's
+      uint32_t c2 = cnt + 1;
       if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
       if (prm.smooth_k) {
-        double sums[8];
-        if (nvalid == 32)
-          chunk_sums<true>(rows, 32, lane, sums);
+        // K tile: exact fp64 chunk sums, the second half's partial sums
+        // joined into the first half's
+        const uint8_t* rows = stage_rows(c2);
+        float2 hi[4], lo[4];
+        uint32_t mx, mn;
+        if (nv == kHalfRows)
+          key_sum_partial<true>(rows, kHalfRows, lane, hi, lo, mx, mn);
         else
-          chunk_sums<false>(rows, nvalid, lane, sums);
-        tc::mbar_arrive(cx.empty(c2 % kStages));
-        ++c2;
-        if (lane < 16) {
+          key_sum_partial<false>(rows, nv, lane, hi, lo, mx, mn);
+        if (sub == 1) {
+          if (lane < 16) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) ks[tw][8 * lane + c] = sums[c];
+            for (int k = 0; k < 4; ++k) {
+              xk_hi[chunk][8 * lane + 2 * k] = hi[k].x;
+              xk_hi[chunk][8 * lane + 2 * k + 1] = hi[k].y;
+              xk_lo[chunk][8 * lane + 2 * k] = lo[k].x;
+              xk_lo[chunk][8 * lane + 2 * k + 1] = lo[k].y;
+            }
+          }
+          if (lane == 0) {
+            xk_bits[chunk][0] = mx;
+            xk_bits[chunk][1] = mn;
+          }
+          pair_bar(pair);
+          tc::mbar_arrive(cx.empty(c2 % kStages));
+        } else {
+          pair_bar(pair);
+          const int cb = 8 * (lane & 15);
+          double sums[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float2 s, e;
+            two_sum2(hi[k], make_float2(xk_hi[chunk][cb + 2 * k], xk_hi[chunk][cb + 2 * k + 1]), s, e);
+            const float2 l = __fadd2_rn(
+                __fadd2_rn(lo[k], make_float2(xk_lo[chunk][cb + 2 * k], xk_lo[chunk][cb + 2 * k + 1])), e);
+            sums[2 * k] = __dadd_rn(static_cast<double>(s.x), static_cast<double>(l.x));
+            sums[2 * k + 1] = __dadd_rn(static_cast<double>(s.y), static_cast<double>(l.y));
+          }
+          if (!key_sum_exact(__vmaxu2(mx, xk_bits[chunk][0]), __vminu2(mn, xk_bits[chunk][1]))) {
+            // this warp's rows are followed by the second half's in the tile
+            const int nvc = valid_rows(S, s0c, kQKBlock);
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) sums[c] = fp64_chunk_sum(rows, nvc, (lane & 15) * 16 + 2 * c);
+          }
+          tc::mbar_arrive(cx.empty(c2 % kStages));
+          if (lane < 16) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ks[chunk][cb + c] = sums[c];
+          }
         }
+        ++c2;
+        if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
       }
       // V tile: max |v| per channel (bf16 magnitudes compare as integers)
-      const uint32_t sv = c2 % kStages;
-      if (c2 != mine && !wait_bar(cx, cx.full(sv), (c2 / kStages) & 1u)) break;
-      const uint8_t* vr = smem + sv * kTileBytes + tw * 32 * 256;
+      const uint8_t* vr = stage_rows(c2);
       const int half = lane >> 4;
       uint32_t m4[4] = {0u, 0u, 0u, 0u};  // channel pairs (8l, 8l+1) .. (8l+6, 8l+7)
-      if (nvalid == 32) {
-#pragma unroll 4
-        for (int i = 0; i < 8; ++i) {
+      if (nv == kHalfRows) {
+#pragma unroll
+        for (int i = 0; i < kHalfRows / 4; ++i) {
           const uint4 wa = tok8(vr, 4 * i + half, lane), wb = tok8(vr, 4 * i + 2 + half, lane);
           m4[0] = __vimax3_u16x2(m4[0], wa.x & kAbs2, wb.x & kAbs2);
           m4[1] = __vimax3_u16x2(m4[1], wa.y & kAbs2, wb.y & kAbs2);
@@ -643,9 +950,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           m4[3] = __vimax3_u16x2(m4[3], wa.w & kAbs2, wb.w & kAbs2);
         }
       } else {
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < kHalfRows / 2; ++i) {
           const int t = 2 * i + half;
-          if (t < nvalid) {
+          if (t < nv) {
             const uint4 w = tok8(vr, t, lane);
             m4[0] = __vmaxu2(m4[0], w.x & kAbs2);
             m4[1] = __vmaxu2(m4[1], w.y & kAbs2);
@@ -654,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc::mbar_arrive(cx.empty(sv));
+      tc::mbar_arrive(cx.empty(c2 % kStages));
 #pragma unroll
       for (int k = 0; k < 4; ++k) m4[k] = __vmaxu2(m4[k], __shfl_xor_sync(0xffffffffu, m4[k], 16));
       if (lane < 16) {
@@ -663,128 +970,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       team_bar(1);
       if (tt < kHeadDim) {
+        // the group's results: levels 1 and 2 of the pairwise tree over its 4
+        // chunk sums, and its max |v| per channel
         const int c = tt;
         const int64_t slot = (bh * G + it.g) * kHeadDim + c;
-        if (prm.smooth_k) {
-          // levels 1..3 of the pairwise tree over the group's 8 chunks
-          const double l0 = __dadd_rn(ks[0][c], ks[1][c]);
-          const double l1 = __dadd_rn(ks[2][c], ks[3][c]);
-          const double l2 = __dadd_rn(ks[4][c], ks[5][c]);
-          const double l3 = __dadd_rn(ks[6][c], ks[7][c]);
-          prm.ksum[slot] = __dadd_rn(__dadd_rn(l0, l1), __dadd_rn(l2, l3));
-        }
+        if (prm.smooth_k) prm.ksum[slot] = __dadd_rn(__dadd_rn(ks[0][c], ks[1][c]), __dadd_rn(ks[2][c], ks[3][c]));
         uint32_t mb = 0u;
 #pragma unroll
         for (int i = 0; i < kWarps; ++i) {
-          const uint32_t pair = vm[i][c >> 1];
-          mb = max(mb, (c & 1) ? (pair >> 16) : (pair & 0xFFFFu));
+          const uint32_t pr = vm[i][c >> 1];
+          mb = max(mb, (c & 1) ? (pr >> 16) : (pr & 0xFFFFu));
         }
         prm.vmax[slot] = __uint_as_float(mb << 16);
-        __threadfence();
       }
       team_bar(1);
-      if (tt == 0) last_flag = atomicAdd(prm.done + bh, 1u) == static_cast<unsigned>(G - 1);
-      team_bar(1);
-      if (last_flag) {
-        // finish the head: the group sums are complete (each writer fenced
-        // before counting itself done)
-        __threadfence();
-        const int c = tt & (kHeadDim - 1), half = tt >> 7;
-        int64_t P = 1;
-        while (P < G) P *= 2;
-        const int64_t lo = half == 0 ? 0 : (P == 1 ? 1 : P / 2);
-        const int64_t hi_end = half == 0 ? (P == 1 ? 1 : P / 2) : P;
-        const int64_t n = max(int64_t(0), min(G, hi_end) - lo);
-        double t = 0.0;
-        if (prm.smooth_k && n > 0) t = tree_sum(prm.ksum + (bh * G + lo) * kHeadDim + c, n);
-        float vmx = 0.0f;
-        for (int64_t gi = lo; gi < lo + n; ++gi) vmx = fmaxf(vmx, __ldcg(prm.vmax + (bh * G + gi) * kHeadDim + c));
-        if (half == 1) {
-          fin_right[c] = t;
-          fin_vmax[c] = vmx;
+      if (tt == 0) {
+        // report the group to the counter warp
+        const uint32_t e = ev_cnt % kEvents;
+        if (wait_bar(cx, cx.evt_empty(e), ((ev_cnt / kEvents) & 1u) ^ 1u)) {
+          evt_bh[e] = bh;
+          tc::mbar_arrive(cx.evt_full(e));
         }
-        team_bar(1);
-        if (half == 0) {
-          float mu = 0.0f;
-          if (prm.smooth_k) {
-            const double total = P > 1 ? __dadd_rn(t, fin_right[c]) : t;
-            mu = __double2float_rn(__ddiv_rn(total, static_cast<double>(S)));
-          }
-          prm.out.k_mean[bh * kHeadDim + c] = mu;
-          prm.out.v_scale[bh * kHeadDim + c] = __fdiv_rn(fmaxf(vmx, fin_vmax[c]), kE4M3Max);
-          __threadfence();
+        ++ev_cnt;
+      }
+    } else if (team == 0) {
+      // codes item, team 0: V codes of this warp's 16 tokens, transposed to
+      // [channel][token] (4-channel lanes); the V scales come with the K tile
+      const float4 svs = *reinterpret_cast<const float4*>(hstat + st * (kHstatBytes / 4) + kHeadDim + 4 * lane);
+      tc::mbar_arrive(cx.empty(st));  // the K tile is team 1's
+      const uint32_t c2 = cnt + 1;
+      if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
+      const uint8_t* rows = stage_rows(c2);
+      const float sc[4] = {svs.x, svs.y, svs.z, svs.w};
+      float rv[4];
+      uint32_t keep = 0u;
+      bool fast = true;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        rv[c] = sc[c] >= FLT_MIN ? __frcp_rn(sc[c]) : 0.0f;
+        if (sc[c] > 0.0f) keep |= 0xFFu << (8 * c);
+        fast = fast && (sc[c] >= FLT_MIN || sc[c] == 0.0f);  // zero channels are masked to code 0
+      }
+      const float2 r01 = make_float2(rv[0], rv[1]), r23 = make_float2(rv[2], rv[3]);
+      uint32_t a[kHalfRows];  // a[t]: the 4 channels' codes of token t
+      uint32_t redo = 0u;     // bit t: token t needs the exact division
+#pragma unroll
+      for (int t = 0; t < kHalfRows; ++t) {
+        a[t] = 0u;
+        if (nv == kHalfRows || t < nv) {
+          uint32_t code;
+          if (!(v_code_quad_fast(tok4(rows, t, lane), r01, r23, code) && fast)) redo |= 1u << t;
+          a[t] = code & keep;
         }
-        team_bar(1);
-        if (tt == 0) {
-          asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(prm.ready + bh), "r"(1u) : "memory");
+      }
+      if (redo != 0u) {
+        // rare: tokens whose fast codes are not certain
+#pragma unroll
+        for (int t = 0; t < kHalfRows; ++t)
+          if ((redo >> t) & 1u) a[t] = exact_v_quad(tok4(rows, t, lane), svs) & keep;
+      }
+      tc::mbar_arrive(cx.empty(c2 % kStages));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        // 4x4 byte transposes: tokens 4j..4j+3 of channel 4*lane+c
+        uint32_t cw[4];
+#pragma unroll
+        for (int j = 0; j < kHalfRows / 4; ++j) {
+          const uint32_t lo01 = __byte_perm(a[4 * j], a[4 * j + 1], (c & 2) ? 0x7362 : 0x5140);
+          const uint32_t lo23 = __byte_perm(a[4 * j + 2], a[4 * j + 3], (c & 2) ? 0x7362 : 0x5140);
+          cw[j] = __byte_perm(lo01, lo23, (c & 1) ? 0x7632 : 0x5410);
         }
+        __stcs(reinterpret_cast<uint4*>(prm.out.vt_codes + (bh * kHeadDim + 4 * lane + c) * S_pad + s0),
+               make_uint4(cw[0], cw[1], cw[2], cw[3]));
       }
     } else {
-      // codes item (the head's key mean and V scales are published)
-      if (team == 1 && !wait_bar(cx, cx.full(mine % kStages), (mine / kStages) & 1u)) break;
-      if (team == 0) {
-        // K codes of k - mean
-        if (in_pad) {
-          int8_t* kc = prm.write_int8 ? prm.out.k_codes + bh * S_pad * kHeadDim : nullptr;
-          uint16_t* k16 = prm.out.k16 + bh * S_pad * kHeadDim;
-          float skv;
-          if (prm.smooth_k) {
-            const float4* mp = reinterpret_cast<const float4*>(prm.out.k_mean + bh * kHeadDim + 8 * (lane & 15));
-            const float4 ma = __ldcg(mp), mb = __ldcg(mp + 1);
-            const float2 nmu[4] = {make_float2(-ma.x, -ma.y), make_float2(-ma.z, -ma.w), make_float2(-mb.x, -mb.y),
-                                   make_float2(-mb.z, -mb.w)};
-            skv = nvalid == 32 ? quantize_block<true, true>(rows, nmu, 32, kc, k16, s0, lane)
-                               : quantize_block<true, false>(rows, nmu, nvalid, kc, k16, s0, lane);
-          } else {
-            const float2 nz[4] = {};
-            skv = nvalid == 32 ? quantize_block<false, true>(rows, nz, 32, kc, k16, s0, lane)
-                               : quantize_block<false, false>(rows, nz, nvalid, kc, k16, s0, lane);
-          }
-          if (lane == 0) prm.out.k_scale[bh * (S_pad / kQKBlock) + s0 / kQKBlock] = skv;
-        }
-        tc::mbar_arrive(cx.empty(st));
-        if (!pass(cnt + 1)) break;
+      // codes item, team 1: K codes of k - mean; the key mean comes with the
+      // K tile
+      int8_t* kc = prm.write_int8 ? prm.out.k_codes + bh * S_pad * kHeadDim : nullptr;
+      uint16_t* k16 = prm.out.k16 + bh * S_pad * kHeadDim;
+      const uint8_t* rows = stage_rows(cnt);
+      float skv;
+      if (prm.smooth_k) {
+        const float4* mp = reinterpret_cast<const float4*>(hstat + st * (kHstatBytes / 4) + 8 * (lane & 15));
+        const float4 ma = mp[0], mb = mp[1];
+        const float2 nmu[4] = {make_float2(-ma.x, -ma.y), make_float2(-ma.z, -ma.w), make_float2(-mb.x, -mb.y),
+                               make_float2(-mb.z, -mb.w)};
+        skv = nv == kHalfRows
+                  ? quantize_half_block<true, true>(rows, nmu, kHalfRows, kc, k16, s0, lane, xm, xo, pair)
+                  : quantize_half_block<true, false>(rows, nmu, nv, kc, k16, s0, lane, xm, xo, pair);
       } else {
-        // V codes, transposed to [channel][token] (4-channel lanes)
-        if (in_pad) {
-          const float4 svs = __ldcg(reinterpret_cast<const float4*>(prm.out.v_scale + bh * kHeadDim + 4 * lane));
-          const float sc[4] = {svs.x, svs.y, svs.z, svs.w};
-          float rv[4];
-          uint32_t keep = 0u;
-          bool fast = true;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            rv[c] = sc[c] >= FLT_MIN ? __frcp_rn(sc[c]) : 0.0f;
-            if (sc[c] > 0.0f) keep |= 0xFFu << (8 * c);
-            fast = fast && (sc[c] >= FLT_MIN || sc[c] == 0.0f);  // zero channels are masked to code 0
-          }
-          const float2 r01 = make_float2(rv[0], rv[1]), r23 = make_float2(rv[2], rv[3]);
-          uint32_t cw[4][8];  // cw[c][j]: tokens 4j..4j+3 of channel 4*lane+c
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t a[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int t = 4 * j + q;
-              a[q] = (nvalid == 32 || t < nvalid) ? v_code_quad(tok4(rows, t, lane), r01, r23, svs, fast) & keep : 0u;
-            }
-            // 4x4 byte transpose: a[q] = token q's channels -> cw[c][j] = channel c's tokens
-            const uint32_t t01l = __byte_perm(a[0], a[1], 0x5140), t01h = __byte_perm(a[0], a[1], 0x7362);
-            const uint32_t t23l = __byte_perm(a[2], a[3], 0x5140), t23h = __byte_perm(a[2], a[3], 0x7362);
-            cw[0][j] = __byte_perm(t01l, t23l, 0x5410);
-            cw[1][j] = __byte_perm(t01l, t23l, 0x7632);
-            cw[2][j] = __byte_perm(t01h, t23h, 0x5410);
-            cw[3][j] = __byte_perm(t01h, t23h, 0x7632);
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint4* dst = reinterpret_cast<uint4*>(prm.out.vt_codes + (bh * kHeadDim + 4 * lane + c) * S_pad + s0);
-            __stcs(dst, make_uint4(cw[c][0], cw[c][1], cw[c][2], cw[c][3]));
-            __stcs(dst + 1, make_uint4(cw[c][4], cw[c][5], cw[c][6], cw[c][7]));
-          }
-        }
-        tc::mbar_arrive(cx.empty(mine % kStages));
+        const float2 nz[4] = {};
+        skv = nv == kHalfRows
+                  ? quantize_half_block<false, true>(rows, nz, kHalfRows, kc, k16, s0, lane, xm, xo, pair)
+                  : quantize_half_block<false, false>(rows, nz, nv, kc, k16, s0, lane, xm, xo, pair);
       }
+      xpar ^= 1;
+      if (sub == 0 && lane == 0) prm.out.k_scale[bh * nblk + s0c / kQKBlock] = skv;
+      tc::mbar_arrive(cx.empty(st));
+      if (!pass(cnt + 1)) break;
     }
     cnt += n_stages;
   }
@@ -795,7 +1078,7 @@ struct ScratchLayout {
 };
 
 ScratchLayout scratch_layout(int64_t B, int64_t S, int64_t H) {
-  const int64_t G = div_up(S, kGroup);
+  const int64_t G = div_up(S, kItemTokens);
   const size_t NH = static_cast<size_t>(B * H);
   const size_t n = NH * static_cast<size_t>(G) * kHeadDim;
   auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -810,7 +1093,7 @@ ScratchLayout scratch_layout(int64_t B, int64_t S, int64_t H) {
 }
 
 // 4-D bf16 map over one input: dims (channel, a1, a2, b) where (a1, a2) are
-// (s, h) or (h, s) in increasing stride order; boxes of 128 channels x 256
+// (s, h) or (h, s) in increasing stride order; boxes of 128 channels x 128
 // tokens. Returns the position of the token axis (1 or 2), or 0 on failure.
 int make_input_map(CUtensorMap* m, const Bf16In& t, int64_t B, int64_t S, int64_t H) {
   const bool s_first = t.ss <= t.sh;
@@ -818,8 +1101,8 @@ int make_input_map(CUtensorMap* m, const Bf16In& t, int64_t B, int64_t S, int64_
                             static_cast<uint64_t>(s_first ? H : S), static_cast<uint64_t>(B)};
   const uint64_t strides[3] = {static_cast<uint64_t>((s_first ? t.ss : t.sh) * 2),
                                static_cast<uint64_t>((s_first ? t.sh : t.ss) * 2), static_cast<uint64_t>(t.sb * 2)};
-  const uint32_t box[4] = {kHeadDim, s_first ? static_cast<uint32_t>(kGroup) : 1u,
-                           s_first ? 1u : static_cast<uint32_t>(kGroup), 1u};
+  const uint32_t box[4] = {kHeadDim, s_first ? static_cast<uint32_t>(kItemTokens) : 1u,
+                           s_first ? 1u : static_cast<uint32_t>(kItemTokens), 1u};
   if (!make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
     return 0;
   return s_first ? 1 : 2;
@@ -839,14 +1122,15 @@ cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, i
   p.S_pad = padded_len(S);
   p.H = H;
   p.NH = B * H;
-  p.G = div_up(S, kGroup);
+  p.G = div_up(S, kItemTokens);
   p.total = 2 * p.NH * p.G;
-  // codes of head h follow the stats of head h + lag: the bytes that pass
-  // through L2 in between (about lag heads of inputs and outputs) must leave
-  // head h's K and V in L2, while lag must exceed the heads in flight
-  const double head_bytes = static_cast<double>(S) * kHeadDim * (3 * 2 + 2 * 1 + 2 * 2 + 1);
-  int64_t lag = static_cast<int64_t>(0.7 * static_cast<double>(l2_bytes_current()) / head_bytes);
-  if (lag < 2) lag = 2;
+  // codes of head h follow the stats of head h + lag: K and V of the heads
+  // in between are held in L2 (evict_last) until their codes items read them
+  // again, so lag heads of K and V should fit in half of L2; a longer lag
+  // also leaves each head's finishing step more time before its codes run
+  const double kv_head_bytes = static_cast<double>(S) * kHeadDim * 2 * 2;
+  int64_t lag = static_cast<int64_t>(0.5 * static_cast<double>(l2_bytes_current()) / kv_head_bytes);
+  if (lag < 1) lag = 1;
   if (lag > p.NH) lag = p.NH;
   p.lag = lag;
   p.smooth_k = smooth_k ? 1 : 0;

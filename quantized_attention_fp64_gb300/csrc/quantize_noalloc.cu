@@ -102,7 +102,7 @@ extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_
     if (p == nullptr) return SAGE_ERR_NULLPTR;
     if (!aligned16(p)) return SAGE_ERR_ALIGN;
   }
-  // the built-in buffer bounds the problem size: B * H * ceil(S / 256) groups
+  // the built-in buffer bounds the problem size: B * H * ceil(S / 128) groups
   // of 128 channels, 12 bytes each (plus alignment)
   if (prologue_scratch_bytes(B, S, H) > kNoAllocScratch) return SAGE_ERR_WORKSPACE;
   void* scratch = noalloc_scratch_ptr(&rc);
