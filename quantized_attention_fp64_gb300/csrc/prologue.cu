@@ -19,9 +19,9 @@
 //     the head as ready.
 //   codes item (head, 128-token group): K codes of k - mean, V codes
 //     (transposed); the producer loads its tiles once the head is ready.
-// The codes items of head h come after the stats items of head h + L, so K
-// and V are read the second time while still in L2 (L is sized from the L2
-// capacity). The producer loads each tensor's 128-token x 128-channel bf16
+// All stats items come before all codes items (the general order, codes of
+// head h after the stats of head h + L, is kept with L = every head; see the
+// launcher for why). The producer loads each tensor's 128-token x 128-channel bf16
 // tile with one 4-D TMA copy into a 6-stage ring (32 KB per stage); an item
 // takes 2 or 3 stages, so the next items' tiles load while one is computed.
 // Two warps share each 32-token block (16 tokens each) and exchange partial
@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::prefetch_tmap(&tm_k);
       tc::prefetch_tmap(&tm_v);
       // Q is read once; K and V are read by the stats item and again by the
-      // codes item lag heads later, so they are kept in L2 until then
+      // codes item, so they are marked to stay in L2 where it has room
       const uint64_t pol_first = tc::policy_evict_first(), pol_last = tc::policy_evict_last();
       uint32_t cnt = 0, stats_pushed = 0, fin_head = 0;
       int pending[kStages];
@@ -1124,14 +1124,12 @@ cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, i
   p.NH = B * H;
   p.G = div_up(S, kItemTokens);
   p.total = 2 * p.NH * p.G;
-  // codes of head h follow the stats of head h + lag: K and V of the heads
-  // in between are held in L2 (evict_last) until their codes items read them
-  // again, so lag heads of K and V should fit in half of L2; a longer lag
-  // also leaves each head's finishing step more time before its codes run
-  const double kv_head_bytes = static_cast<double>(S) * kHeadDim * 2 * 2;
-  int64_t lag = static_cast<int64_t>(0.5 * static_cast<double>(l2_bytes_current()) / kv_head_bytes);
-  if (lag < 1) lag = 1;
-  if (lag > p.NH) lag = p.NH;
+  // every stats item comes before every codes item (lag = all heads).
+  // Interleaving them (codes of head h right after the stats of head h + L,
+  // to read K and V the second time from L2) was measured slower at every L:
+  // the codes items then wait for heads still being finished, and those
+  // waits cost more than the DRAM reads they save
+  const int64_t lag = p.NH;
   p.lag = lag;
   p.smooth_k = smooth_k ? 1 : 0;
   p.write_int8 = write_int8 ? 1 : 0;
