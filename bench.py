@@ -32,7 +32,23 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = "B1_H28_S16384"
+# DRAM traffic of one attention launch at this workload (dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture), valid only for the kernel source
+# it was taken on: reported when the source's SHA-256 prefix still matches.
+ATTN_TRAFFIC = {"bytes": 294207744 + 92270592, "source_sha256": "d437e99b2da76514",
+                "capture": "ncu --set full, profiles/attention_tc_B1_H28_S16384.md"}
 PROLOGUE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def attention_traffic():
+    """The recorded per-launch DRAM traffic of the attention kernel, or None
+    once its source differs from the one the counters were taken on."""
+    import hashlib
+
+    path = os.path.join(ROOT, "quantized_attention_fp64_gb300", "csrc", "attention_tc.cu")
+    with open(path, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return ATTN_TRAFFIC["bytes"] if digest.startswith(ATTN_TRAFFIC["source_sha256"]) else None
 
 
 def load_peaks():
@@ -356,7 +372,8 @@ def run_gpu(args):
                    "l2": "inputs (3 x 117 MB) larger than L2; no flush",
                    "parallelism": f"replicas x{world} (heads are independent)"},
         "roofline": {"kernel": "attention_tc", "bound": "tensor", "achieved": att_tflops, "peak": p_att,
-                     "unit": "TFLOP/s", "frac": att_tflops / p_att, "traffic": None,
+                     "unit": "TFLOP/s", "frac": att_tflops / p_att, "traffic": attention_traffic(),
+                     "traffic_unit": "bytes per launch (DRAM read + write, one ncu capture)",
                      "peak_note": f"harmonic mean of fp16 {p16:.1f} and e4m3 {p8:.1f} TFLOP/s "
                                   f"({peak_kind} bf16 burst: the kernel is timed alone; e4m3 = 2x nominal ratio)"},
         "attention_kernel": {"ms": t_att * 1e3, "tflops": att_tflops, "frac_of_peak": att_tflops / p_att},
