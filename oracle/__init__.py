@@ -20,4 +20,5 @@ from .sage_oracle import (  # noqa: F401
     quantize_head,
     quantize_int8_blocks,
     quantize_v_channels,
+    smooth_k_lse_term,
 )

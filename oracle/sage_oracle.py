@@ -255,8 +255,19 @@ def quantize_head(q32, k32, v32, smooth_k: bool):
 # Attention
 # ----------------------------------------------------------------------------
 
+def _visible(rows, j0, j1, causal):
+    """Key mask of one tile for the selected query rows: True where key j may
+    be attended to. Without a mask every key is visible; with the causal mask
+    query i sees keys j <= i (Q and K have the same length, so the mask is
+    the lower triangle)."""
+    if not causal:
+        return None
+    return np.arange(j0, j1)[None, :] <= np.asarray(rows)[:, None]
+
+
 def attention_emulated(q_codes, k_codes, v_vals, q_scale, k_scale, v_scale, sm_scale,
-                       rows=None, quantize_p: bool = True, return_fp32: bool = False):
+                       rows=None, quantize_p: bool = True, return_fp32: bool = False,
+                       causal: bool = False, return_lse: bool = False, lse_term=None):
     """Quantized flash attention for one (batch, head), emulated step by step.
 
     [IX] "The kernel": QK^T in INT8 with 32-bit integer accumulation, PV in
@@ -264,7 +275,8 @@ def attention_emulated(q_codes, k_codes, v_vals, q_scale, k_scale, v_scale, sm_s
     ascending key order (reading):
 
     1. S_ij = sum_d qc_id * kc_jd, exact integers.
-    2. logit_ij = fl32(S_ij) * c_ij, c_ij = (s_q[i/32] * s_k[j/32]) * sm_scale (fp32).
+    2. logit_ij = fl32(S_ij) * c_ij, c_ij = (s_q[i/32] * s_k[j/32]) * sm_scale (fp32);
+       keys the causal mask hides get -inf.
     3. m' = max(m, max_j logit_ij); alpha = exp(m - m'); p_ij = exp(logit_ij - m')
        (the differences in fp32, exp evaluated in fp64 and rounded to fp32).
     4. l = alpha * l + sum_j p_ij, from the unquantized p (tile sum in fp64,
@@ -276,11 +288,26 @@ def attention_emulated(q_codes, k_codes, v_vals, q_scale, k_scale, v_scale, sm_s
 
     Finally O_id = ((acc_d / l) * s_v[d]) / 448 in fp32, rounded to bf16.
 
+    A tile the causal mask hides completely leaves m, l and acc unchanged
+    (alpha = 1, p = 0), so skipping it, as a kernel does, gives the same
+    result.
+
+    Log-sum-exp (``return_lse``; the pages name the flag, not its meaning).
+    Reading: the natural log of sum_j exp(sm_scale * q_i . k_j) over the keys
+    row i sees, as fp32, which is what lets partial attention results over
+    disjoint key sets be merged. From the emulation it is m + ln(l), the
+    log-sum-exp of the logits of the codes. The K codes are of k - mean when
+    smooth_k is on; a per-channel key shift changes every logit of row i by
+    the same sm_scale * q_i . mean, so ``lse_term`` (see smooth_k_lse_term)
+    is added to restore the log-sum-exp of the original keys:
+    lse_i = m_i + ln(l_i) + lse_term_i, in fp64, rounded to fp32.
+
     q_codes, k_codes: [S, D] integer codes (or float values for the
     identity-quantization pin); v_vals: float32 [S, D] decoded V codes;
     q_scale, k_scale: float32 [ceil(S/32)]; v_scale: float32 [D].
     Returns bf16-rounded float32 [R, D] for the selected query rows, or the
-    fp32 values before that rounding when ``return_fp32``.
+    fp32 values before that rounding when ``return_fp32``; with
+    ``return_lse`` a pair (output, lse float32 [R]).
     """
     k_codes = np.asarray(k_codes)
     s_len, d = k_codes.shape
@@ -300,9 +327,13 @@ def attention_emulated(q_codes, k_codes, v_vals, q_scale, k_scale, v_scale, sm_s
         s_ij = qc @ k_codes[j0:j1].astype(_F64).T
         c = ((sq[:, None] * sk[np.arange(j0, j1) // QK_BLOCK][None, :]).astype(_F32) * scale).astype(_F32)
         logit = (s_ij.astype(_F32) * c).astype(_F32)
+        vis = _visible(rows, j0, j1, causal)
+        if vis is not None:
+            logit = np.where(vis, logit, _F32(-np.inf)).astype(_F32)
         m_new = np.maximum(m, logit.max(axis=1))
         with np.errstate(invalid="ignore"):
             alpha = np.exp((m - m_new).astype(_F64)).astype(_F32)
+        alpha = np.where(m == m_new, _F32(1.0), alpha).astype(_F32)  # also for -inf - (-inf)
         p = np.exp((logit - m_new[:, None]).astype(_F32).astype(_F64)).astype(_F32)
         l = (alpha * l + p.astype(_F64).sum(axis=1).astype(_F32)).astype(_F32)
         p448 = (_F32(P_SCALE) * p).astype(_F32)
@@ -311,15 +342,32 @@ def attention_emulated(q_codes, k_codes, v_vals, q_scale, k_scale, v_scale, sm_s
         acc = (alpha[:, None] * acc + pv).astype(_F32)
         m = m_new
     out = ((((acc / l[:, None]).astype(_F32)) * sv[None, :]).astype(_F32) / _F32(P_SCALE)).astype(_F32)
-    return out if return_fp32 else bf16_round(out)
+    out = out if return_fp32 else bf16_round(out)
+    if not return_lse:
+        return out
+    term = np.zeros(n_rows, dtype=_F64) if lse_term is None else np.asarray(lse_term, dtype=_F64)
+    lse = (m.astype(_F64) + np.log(l.astype(_F64)) + term).astype(_F32)
+    return out, lse
 
 
-def attention_exact(q32, k32, v32, sm_scale, rows=None) -> np.ndarray:
+def smooth_k_lse_term(q32, k_mean, sm_scale, rows=None) -> np.ndarray:
+    """The log-sum-exp term of smooth_k: sm_scale * q_i . mean for each query
+    row, with the bf16 query values (not their codes, which would add the Q
+    quantization error) and the fp32 key mean, in fp64. Zero when the mean is
+    zero (smooth_k off)."""
+    q32 = np.asarray(q32, dtype=_F32)
+    rows = np.arange(q32.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    return _F64(_F32(sm_scale)) * (q32[rows].astype(_F64) @ np.asarray(k_mean, dtype=_F32).astype(_F64))
+
+
+def attention_exact(q32, k32, v32, sm_scale, rows=None, causal: bool = False, return_lse: bool = False):
     """Exact softmax attention in fp64 for one (batch, head), no quantization.
 
-    O = softmax(sm_scale * Q K^T) V over all S keys (no mask, not causal:
-    [CA] "原因分析"), with the logits, the two-pass softmax and the product
-    with V all in fp64. Inputs are the bf16 values as float32 [S, D].
+    O = softmax(sm_scale * Q K^T) V over all S keys ([CA] "原因分析": no mask,
+    not causal), or with ``causal`` over the keys j <= i, with the logits,
+    the two-pass softmax and the product with V all in fp64. Inputs are the
+    bf16 values as float32 [S, D]. With ``return_lse`` also the natural-log
+    log-sum-exp of each row's logits (fp64).
     """
     q32 = np.asarray(q32, dtype=_F32)
     rows = np.arange(q32.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
@@ -327,6 +375,12 @@ def attention_exact(q32, k32, v32, sm_scale, rows=None) -> np.ndarray:
     kf = np.asarray(k32, dtype=_F32).astype(_F64)
     vf = np.asarray(v32, dtype=_F32).astype(_F64)
     logits = (qf @ kf.T) * _F64(_F32(sm_scale))
+    if causal:
+        logits = np.where(np.arange(kf.shape[0])[None, :] <= rows[:, None], logits, -np.inf)
     m = logits.max(axis=1, keepdims=True)
     p = np.exp(logits - m)
-    return (p @ vf) / p.sum(axis=1, keepdims=True)
+    z = p.sum(axis=1, keepdims=True)
+    out = (p @ vf) / z
+    if return_lse:
+        return out, (m + np.log(z))[:, 0]
+    return out

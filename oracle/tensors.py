@@ -23,6 +23,7 @@ from .sage_oracle import (
     attention_exact,
     e4m3_decode,
     quantize_head,
+    smooth_k_lse_term,
 )
 
 
@@ -83,16 +84,26 @@ def quantize_tensors(q, k, v, layout: str = "NHD", smooth_k: bool = True, heads=
 
 
 def attention_from_codes(qz, s_len: int, sm_scale: float, b: int, h: int, rows=None,
-                         return_fp32: bool = False):
+                         return_fp32: bool = False, causal: bool = False, return_lse: bool = False,
+                         q=None, layout: str = "NHD"):
     """Emulated attention of one (batch, head) from a quantized bundle
-    laid out as :func:`quantize_tensors` returns it."""
+    laid out as :func:`quantize_tensors` returns it. With ``return_lse`` the
+    pair (output, lse); when the bf16 query tensor ``q`` is given, the lse
+    includes the smooth_k term from the bundle's key mean (the log-sum-exp of
+    the original keys), otherwise it is that of the mean-reduced keys."""
     vt = qz["vt_codes"][b, h, :, :s_len]
     v_vals = e4m3_decode(vt.T)
+    term = None
+    if return_lse and q is not None:
+        term = smooth_k_lse_term(head_view(q, layout, b, h), qz["k_mean"][b, h], sm_scale, rows=rows)
     return attention_emulated(qz["q_codes"][b, h, :s_len], qz["k_codes"][b, h, :s_len], v_vals,
                               qz["q_scale"][b, h], qz["k_scale"][b, h], qz["v_scale"][b, h],
-                              sm_scale, rows=rows, return_fp32=return_fp32)
+                              sm_scale, rows=rows, return_fp32=return_fp32, causal=causal,
+                              return_lse=return_lse, lse_term=term)
 
 
-def exact_head(q, k, v, layout: str, sm_scale: float, b: int, h: int, rows=None):
+def exact_head(q, k, v, layout: str, sm_scale: float, b: int, h: int, rows=None, causal: bool = False,
+               return_lse: bool = False):
     return attention_exact(head_view(q, layout, b, h), head_view(k, layout, b, h),
-                           head_view(v, layout, b, h), sm_scale, rows=rows)
+                           head_view(v, layout, b, h), sm_scale, rows=rows, causal=causal,
+                           return_lse=return_lse)
