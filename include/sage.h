@@ -199,13 +199,42 @@ SAGE_API int sage_attention(const sage_quantized* in, int64_t B, int64_t S, int6
                    float sm_scale, void* out_dev, int64_t ob, int64_t os, int64_t oh,
                    void* cuda_stream);
 
-/* Same contract and result tolerance as sage_attention, computed by a plain
- * SIMT kernel (integer dot products, one thread per query row). It exists to
- * cross-check the tensor-core kernel in tests; it is never used as a
- * fallback. */
+/* sage_attention with the two flags the sageattn entry of the pages names
+ * but rejects ("aiter-sage-attention ... #1222", section "What I have so
+ * far": is_causal, return_lse); the page gives their names, not their
+ * meaning, so this library reads them as follows.
+ *  - is_causal != 0: query i attends to keys j <= i only (Q and K have the
+ *    same length, so the mask is the lower triangle). Key tiles a query tile
+ *    cannot see are skipped, which gives the same result as masking them.
+ *  - lse_dev != NULL: fp32 [B][H][S] (contiguous, 4-byte aligned, caller
+ *    owned) receives each query row's natural-log log-sum-exp of its scaled
+ *    logits, ln sum_j exp(sm_scale * q_i . k_j) over the keys it sees, from
+ *    the same online softmax: lse = m + ln(l). The logits are those of the
+ *    bundle's K codes, i.e. of k - mean when the bundle was quantized with
+ *    smooth_k; sage_lse_smooth_k_term adds the term that restores the keys'
+ *    own log-sum-exp (sage_sageattn_ex does so itself).
+ * Errors: as sage_attention, and ALIGN for a misaligned lse_dev. */
+SAGE_API int sage_attention_ex(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D,
+                               float sm_scale, int is_causal, void* out_dev, int64_t ob, int64_t os, int64_t oh,
+                               float* lse_dev, void* cuda_stream);
+
+/* Adds the smooth_k term to a log-sum-exp: lse[b][h][i] += sm_scale *
+ * sum_d q[b, i, h, d] * k_mean[b][h][d], with the BF16 query q (strides as
+ * for sage_quantize) and the bundle's key mean k_mean_dev (fp32 [B][H][128],
+ * 16-byte aligned). A per-channel key shift moves every logit of row i by the
+ * same amount, so this turns the log-sum-exp of the mean-reduced keys into
+ * that of the original keys. Enqueued on cuda_stream (one kernel).
+ * Errors: NULLPTR, SHAPE, HEAD_DIM, ALIGN, ARG, TOO_LARGE, ARCH, CUDA. */
+SAGE_API int sage_lse_smooth_k_term(const sage_bf16_tensor* q, const float* k_mean_dev, int64_t B, int64_t S,
+                                    int64_t H, int64_t D, float sm_scale, float* lse_dev, void* cuda_stream);
+
+/* Same contract and result tolerance as sage_attention_ex, computed by a
+ * plain SIMT kernel (integer dot products, one thread per query row). It
+ * exists to cross-check the tensor-core kernel in tests; it is never used as
+ * a fallback. */
 SAGE_API int sage_attention_simt(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D,
-                        float sm_scale, void* out_dev, int64_t ob, int64_t os, int64_t oh,
-                        void* cuda_stream);
+                        float sm_scale, int is_causal, void* out_dev, int64_t ob, int64_t os, int64_t oh,
+                        float* lse_dev, void* cuda_stream);
 
 /* The sageattn-shaped entry: quantize q, k, v into the workspace, then run
  * attention into out. Shapes and strides are given in the order of
@@ -225,6 +254,20 @@ SAGE_API int sage_sageattn(const void* q_dev, const void* k_dev, const void* v_d
                   int is_causal, float sm_scale, int return_lse, int smooth_k,
                   void* out_dev, const int64_t out_strides[4], int out_dtype,
                   void* workspace_dev, size_t workspace_bytes, void* cuda_stream);
+
+/* sage_sageattn with is_causal and return_lse honoured instead of rejected
+ * (their reading: see sage_attention_ex). When lse_dev is not NULL it
+ * receives the log-sum-exp of the original keys: with smooth_k on, the
+ * key-mean term is added (sage_lse_smooth_k_term). All other arguments,
+ * checks and errors are those of sage_sageattn (except CAUSAL and LSE), and
+ * ALIGN for a misaligned lse_dev. */
+SAGE_API int sage_sageattn_ex(const void* q_dev, const void* k_dev, const void* v_dev,
+                              const int64_t q_shape[4], const int64_t k_shape[4], const int64_t v_shape[4],
+                              const int64_t q_strides[4], const int64_t k_strides[4], const int64_t v_strides[4],
+                              int q_dtype, int k_dtype, int v_dtype, const char* tensor_layout, int is_causal,
+                              float sm_scale, int smooth_k, void* out_dev, const int64_t out_strides[4],
+                              int out_dtype, float* lse_dev, void* workspace_dev, size_t workspace_bytes,
+                              void* cuda_stream);
 
 /* ---------------------------------------------------------- diagnostics -- */
 

@@ -12,8 +12,10 @@ from .api import (  # noqa: F401
     attention,
     attention_simt,
     device_error,
+    lse_smooth_k_term,
     quantize,
     quantize_scratch_size,
     sageattn,
+    sageattn_ex,
     workspace_size,
 )

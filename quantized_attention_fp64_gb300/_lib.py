@@ -39,11 +39,18 @@ _SIGNATURES = {
                                                                         ctypes.POINTER(Quantized), c_vp]),
     "sage_attention": (c_int, [ctypes.POINTER(Quantized), c_i64, c_i64, c_i64, c_i64, ctypes.c_float, c_vp,
                                c_i64, c_i64, c_i64, c_vp]),
-    "sage_attention_simt": (c_int, [ctypes.POINTER(Quantized), c_i64, c_i64, c_i64, c_i64, ctypes.c_float, c_vp,
-                                    c_i64, c_i64, c_i64, c_vp]),
+    "sage_attention_ex": (c_int, [ctypes.POINTER(Quantized), c_i64, c_i64, c_i64, c_i64, ctypes.c_float, c_int,
+                                  c_vp, c_i64, c_i64, c_i64, c_vp, c_vp]),
+    "sage_attention_simt": (c_int, [ctypes.POINTER(Quantized), c_i64, c_i64, c_i64, c_i64, ctypes.c_float, c_int,
+                                    c_vp, c_i64, c_i64, c_i64, c_vp, c_vp]),
+    "sage_lse_smooth_k_term": (c_int, [ctypes.POINTER(Bf16Tensor), c_vp, c_i64, c_i64, c_i64, c_i64, ctypes.c_float,
+                                       c_vp, c_vp]),
     "sage_sageattn": (c_int, [c_vp, c_vp, c_vp, I64x4, I64x4, I64x4, I64x4, I64x4, I64x4, c_int, c_int, c_int,
                               ctypes.c_char_p, c_int, ctypes.c_float, c_int, c_int, c_vp, I64x4, c_int, c_vp,
                               ctypes.c_size_t, c_vp]),
+    "sage_sageattn_ex": (c_int, [c_vp, c_vp, c_vp, I64x4, I64x4, I64x4, I64x4, I64x4, I64x4, c_int, c_int, c_int,
+                                 ctypes.c_char_p, c_int, ctypes.c_float, c_int, c_vp, I64x4, c_int, c_vp, c_vp,
+                                 ctypes.c_size_t, c_vp]),
     "sage_device_error": (c_int, [c_vp, ctypes.POINTER(c_int)]),
     "sage_strerror": (ctypes.c_char_p, [c_int]),
 }

@@ -163,7 +163,8 @@ def quantize(q, k, v, tensor_layout: str = "NHD", smooth_k: bool = True, out: Qu
     return qz
 
 
-def _attention(fn_name: str, qz: QuantizedQKV, sm_scale, tensor_layout: str, out):
+def _attention(fn_name: str, qz: QuantizedQKV, sm_scale, tensor_layout: str, out, is_causal=False,
+               return_lse=False):
     lib = _lib.load()
     B, S, H = qz.B, qz.S, qz.H
     device = qz.buffer.device
@@ -173,20 +174,48 @@ def _attention(fn_name: str, qz: QuantizedQKV, sm_scale, tensor_layout: str, out
     scale = (1.0 / math.sqrt(128.0)) if sm_scale is None else float(sm_scale)
     ob, os_, oh = _bsh_strides(out, tensor_layout)
     bundle = qz.c_struct()
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=device) if return_lse else None
     with torch.cuda.device(device):
-        _check(getattr(lib, fn_name)(ctypes.byref(bundle), B, S, H, 128, ctypes.c_float(scale),
-                                     ctypes.c_void_p(out.data_ptr()), ob, os_, oh, _stream(device)))
-    return out
+        if fn_name == "sage_attention":
+            _check(lib.sage_attention(ctypes.byref(bundle), B, S, H, 128, ctypes.c_float(scale),
+                                      ctypes.c_void_p(out.data_ptr()), ob, os_, oh, _stream(device)))
+        else:
+            _check(getattr(lib, fn_name)(ctypes.byref(bundle), B, S, H, 128, ctypes.c_float(scale),
+                                         int(bool(is_causal)), ctypes.c_void_p(out.data_ptr()), ob, os_, oh,
+                                         ctypes.c_void_p(lse.data_ptr() if lse is not None else None),
+                                         _stream(device)))
+    return (out, lse) if return_lse else out
 
 
-def attention(qz: QuantizedQKV, sm_scale=None, tensor_layout: str = "NHD", out=None) -> torch.Tensor:
-    """Tensor-core attention (sage_attention) on a quantized bundle."""
-    return _attention("sage_attention", qz, sm_scale, tensor_layout, out)
+def attention(qz: QuantizedQKV, sm_scale=None, tensor_layout: str = "NHD", out=None, is_causal: bool = False,
+              return_lse: bool = False):
+    """Tensor-core attention on a quantized bundle: sage_attention, or
+    sage_attention_ex when a causal mask or the log-sum-exp is asked for
+    (then it returns (out, lse) with lse fp32 [B, H, S], the log-sum-exp of
+    the bundle's logits; see lse_smooth_k_term)."""
+    if not is_causal and not return_lse:
+        return _attention("sage_attention", qz, sm_scale, tensor_layout, out)
+    return _attention("sage_attention_ex", qz, sm_scale, tensor_layout, out, is_causal, return_lse)
 
 
-def attention_simt(qz: QuantizedQKV, sm_scale=None, tensor_layout: str = "NHD", out=None) -> torch.Tensor:
+def attention_simt(qz: QuantizedQKV, sm_scale=None, tensor_layout: str = "NHD", out=None, is_causal: bool = False,
+                   return_lse: bool = False):
     """The SIMT cross-check kernel (sage_attention_simt); for tests."""
-    return _attention("sage_attention_simt", qz, sm_scale, tensor_layout, out)
+    return _attention("sage_attention_simt", qz, sm_scale, tensor_layout, out, is_causal, return_lse)
+
+
+def lse_smooth_k_term(q: torch.Tensor, qz: QuantizedQKV, lse: torch.Tensor, sm_scale=None,
+                      tensor_layout: str = "NHD") -> torch.Tensor:
+    """Adds sm_scale * q_i . k_mean to lse in place (sage_lse_smooth_k_term):
+    the log-sum-exp of the mean-reduced keys becomes that of the original keys."""
+    _require_cuda(q)
+    lib = _lib.load()
+    scale = (1.0 / math.sqrt(128.0)) if sm_scale is None else float(sm_scale)
+    with torch.cuda.device(q.device):
+        _check(lib.sage_lse_smooth_k_term(ctypes.byref(_bf16_tensor(q, tensor_layout)),
+                                          ctypes.c_void_p(qz.k_mean.data_ptr()), qz.B, qz.S, qz.H, 128,
+                                          ctypes.c_float(scale), ctypes.c_void_p(lse.data_ptr()), _stream(q.device)))
+    return lse
 
 
 def sageattn(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm_scale=None,
@@ -228,6 +257,48 @@ def sageattn(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm_sc
             ctypes.c_void_p(ws_ptr), ws_n, _stream(q.device))
     _check(rc)
     return out
+
+
+def sageattn_ex(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm_scale=None,
+                return_lse: bool = False, smooth_k: bool = True, out=None, workspace=None):
+    """sageattn with is_causal and return_lse honoured (sage_sageattn_ex):
+    returns out, or (out, lse) with lse fp32 [B, H, S], the natural-log
+    log-sum-exp of each query row's scaled logits. Other unsupported inputs
+    raise SageError as in sageattn."""
+    _require_cuda(q, k, v)
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise SageError(SAGE_ERR_SHAPE, "q, k and v must be 4-d")
+    lib = _lib.load()
+    layout = tensor_layout if isinstance(tensor_layout, str) else str(tensor_layout)
+    B, S, H, D = _bsh(q.shape, layout)
+    ws_bytes = ctypes.c_size_t(0)
+    sizes_ok = lib.sage_workspace_size(B, S, H, D, ctypes.byref(ws_bytes)) == 0
+    proceed = (sizes_ok and layout in ("NHD", "HND") and q.dtype == k.dtype == v.dtype == torch.bfloat16
+               and tuple(q.shape) == tuple(k.shape) == tuple(v.shape))
+    lse = None
+    with torch.cuda.device(q.device):
+        if proceed and out is None:
+            out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+        if proceed and (workspace is None or workspace.numel() < ws_bytes.value):
+            workspace = torch.empty(max(ws_bytes.value, 256), dtype=torch.uint8, device=q.device)
+        if proceed and return_lse:
+            lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+        out_ptr = out.data_ptr() if out is not None else None
+        out_strides = out.stride() if out is not None else (0, 0, 0, 1)
+        out_dtype = _dtype_code(out) if out is not None else 0
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_n = workspace.numel() if workspace is not None else 0
+        scale = float("nan") if sm_scale is None else float(sm_scale)
+        rc = lib.sage_sageattn_ex(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+            _lib.I64x4(*q.shape), _lib.I64x4(*k.shape), _lib.I64x4(*v.shape),
+            _lib.I64x4(*q.stride()), _lib.I64x4(*k.stride()), _lib.I64x4(*v.stride()),
+            _dtype_code(q), _dtype_code(k), _dtype_code(v), layout.encode(), int(bool(is_causal)),
+            ctypes.c_float(scale), int(bool(smooth_k)), ctypes.c_void_p(out_ptr), _lib.I64x4(*out_strides),
+            out_dtype, ctypes.c_void_p(lse.data_ptr() if lse is not None else None),
+            ctypes.c_void_p(ws_ptr), ws_n, _stream(q.device))
+    _check(rc)
+    return (out, lse) if return_lse else out
 
 
 def device_error(device=None) -> int:

@@ -147,25 +147,31 @@ int check_out(const void* out, int64_t ob, int64_t os, int64_t oh) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA; }
 
-typedef cudaError_t (*AttnLaunch)(const Bundle&, int64_t, int64_t, int64_t, float, const Out&, int*, cudaStream_t);
+typedef cudaError_t (*AttnLaunch)(const Bundle&, int64_t, int64_t, int64_t, float, const Out&, bool, float*, int*,
+                                  cudaStream_t);
 
-cudaError_t simt_adapter(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm, const Out& o, int*,
-                         cudaStream_t st) {
-  return launch_attention_simt(in, B, S, H, sm, o, st);
+cudaError_t simt_adapter(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm, const Out& o, bool causal,
+                         float* lse, int*, cudaStream_t st) {
+  return launch_attention_simt(in, B, S, H, sm, o, causal, lse, st);
 }
 
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
 int attention_common(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
-                     void* out_dev, int64_t ob, int64_t os, int64_t oh, void* stream, AttnLaunch launch) {
+                     bool causal, void* out_dev, int64_t ob, int64_t os, int64_t oh, float* lse_dev, void* stream,
+                     AttnLaunch launch) {
   int rc = check_sizes(B, S, H, D);
   if (rc != SAGE_OK) return rc;
   if ((rc = check_bundle(in, false)) != SAGE_OK) return rc;
   if ((rc = check_out(out_dev, ob, os, oh)) != SAGE_OK) return rc;
+  if (lse_dev != nullptr && !aligned4(lse_dev)) return SAGE_ERR_ALIGN;
   if (!std::isfinite(sm_scale) || !(sm_scale > 0.0f)) return SAGE_ERR_ARG;
   int dev = 0;
   if ((rc = check_device(&dev)) != SAGE_OK) return rc;
   if (B == 0 || H == 0 || S == 0) return SAGE_OK;
   Out o{static_cast<uint16_t*>(out_dev), ob, os, oh};
-  return cuda_status(launch(to_bundle(in), B, S, H, sm_scale, o, g_err_ptr[dev], static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch(to_bundle(in), B, S, H, sm_scale, o, causal, lse_dev, g_err_ptr[dev],
+                            static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -176,6 +182,80 @@ int* device_error_ptr() {
   return g_err_ptr[dev];
 }
 
+}  // namespace sage
+
+namespace sage {
+namespace {
+
+// The sageattn path after the checks that differ between the two entries:
+// prologue into the workspace, attention (causal, lse as given), and with
+// lse and smooth_k the key-mean term of the log-sum-exp.
+int sageattn_impl(const void* q_dev, const void* k_dev, const void* v_dev, const int64_t q_shape[4],
+                  const int64_t k_shape[4], const int64_t v_shape[4], const int64_t q_strides[4],
+                  const int64_t k_strides[4], const int64_t v_strides[4], int q_dtype, int k_dtype, int v_dtype,
+                  const char* tensor_layout, bool causal, float sm_scale, float* lse_dev, int smooth_k,
+                  void* out_dev, const int64_t out_strides[4], int out_dtype, void* workspace_dev,
+                  size_t workspace_bytes, void* cuda_stream) {
+  if (q_dtype != SAGE_DTYPE_BF16 || k_dtype != SAGE_DTYPE_BF16 || v_dtype != SAGE_DTYPE_BF16 ||
+      out_dtype != SAGE_DTYPE_BF16)
+    return SAGE_ERR_DTYPE;
+  if (q_shape == nullptr || k_shape == nullptr || v_shape == nullptr || q_strides == nullptr ||
+      k_strides == nullptr || v_strides == nullptr || out_strides == nullptr || tensor_layout == nullptr)
+    return SAGE_ERR_NULLPTR;
+  int is_nhd;
+  if (std::strcmp(tensor_layout, "NHD") == 0) is_nhd = 1;
+  else if (std::strcmp(tensor_layout, "HND") == 0) is_nhd = 0;
+  else return SAGE_ERR_LAYOUT;
+  // axis positions of (b, s, h, d) in the given layout
+  const int ax_s = is_nhd ? 1 : 2, ax_h = is_nhd ? 2 : 1;
+  const int64_t B = q_shape[0], S = q_shape[ax_s], H = q_shape[ax_h], D = q_shape[3];
+  if (D != kHeadDim && D >= 0) return SAGE_ERR_HEAD_DIM;
+  for (int i = 0; i < 4; ++i)
+    if (k_shape[i] != q_shape[i] || v_shape[i] != q_shape[i]) return SAGE_ERR_SHAPE;
+  int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  const int64_t* st[4] = {q_strides, k_strides, v_strides, out_strides};
+  for (int i = 0; i < 4; ++i)
+    if (st[i][3] != 1) return SAGE_ERR_LAYOUT;
+  if (!(std::isnan(sm_scale) || (std::isfinite(sm_scale) && sm_scale > 0.0f))) return SAGE_ERR_ARG;
+  const float scale = std::isnan(sm_scale) ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) : sm_scale;
+  const sage_bf16_tensor qt{q_dev, q_strides[0], q_strides[ax_s], q_strides[ax_h]};
+  const sage_bf16_tensor kt{k_dev, k_strides[0], k_strides[ax_s], k_strides[ax_h]};
+  const sage_bf16_tensor vt{v_dev, v_strides[0], v_strides[ax_s], v_strides[ax_h]};
+  if ((rc = check_bf16_in(&qt)) != SAGE_OK || (rc = check_bf16_in(&kt)) != SAGE_OK ||
+      (rc = check_bf16_in(&vt)) != SAGE_OK)
+    return rc;
+  if ((rc = check_out(out_dev, out_strides[0], out_strides[ax_s], out_strides[ax_h])) != SAGE_OK) return rc;
+  if (lse_dev != nullptr && !aligned4(lse_dev)) return SAGE_ERR_ALIGN;
+  if (workspace_dev == nullptr) return SAGE_ERR_NULLPTR;
+  if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return SAGE_ERR_ALIGN;
+  const BundleLayout bl = bundle_layout(B, S, H);
+  const size_t scratch = prologue_scratch_bytes(B, S, H);
+  if (workspace_bytes < bl.total + scratch) return SAGE_ERR_WORKSPACE;
+  int dev = 0;
+  if ((rc = check_device(&dev)) != SAGE_OK) return rc;
+  if (B == 0 || H == 0 || S == 0) return SAGE_OK;
+  const Bundle bundle = carve(workspace_dev, bl);
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  const Bf16In qi{static_cast<const uint16_t*>(q_dev), qt.stride_b, qt.stride_s, qt.stride_h};
+  const Bf16In ki{static_cast<const uint16_t*>(k_dev), kt.stride_b, kt.stride_s, kt.stride_h};
+  const Bf16In vi{static_cast<const uint16_t*>(v_dev), vt.stride_b, vt.stride_s, vt.stride_h};
+  // the int8 Q/K codes are not read by the attention kernel, so this path
+  // keeps only their fp16 copies
+  if ((rc = cuda_status(launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, bundle,
+                                        static_cast<char*>(workspace_dev) + bl.total, false, g_err_ptr[dev],
+                                        stream))) != SAGE_OK)
+    return rc;
+  const Out o{static_cast<uint16_t*>(out_dev), out_strides[0], out_strides[ax_s], out_strides[ax_h]};
+  if ((rc = cuda_status(launch_attention_tc(bundle, B, S, H, scale, o, causal, lse_dev, g_err_ptr[dev], stream))) !=
+      SAGE_OK)
+    return rc;
+  if (lse_dev != nullptr && smooth_k != 0)
+    return cuda_status(launch_lse_smooth_k_term(qi, bundle.k_mean, B, S, H, scale, lse_dev, stream));
+  return SAGE_OK;
+}
+
+}  // namespace
 }  // namespace sage
 
 using namespace sage;
@@ -245,12 +325,38 @@ int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k, const sa
 
 int sage_attention(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
                    void* out_dev, int64_t ob, int64_t os, int64_t oh, void* cuda_stream) {
-  return attention_common(in, B, S, H, D, sm_scale, out_dev, ob, os, oh, cuda_stream, launch_attention_tc);
+  return attention_common(in, B, S, H, D, sm_scale, false, out_dev, ob, os, oh, nullptr, cuda_stream,
+                          launch_attention_tc);
+}
+
+int sage_attention_ex(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
+                      int is_causal, void* out_dev, int64_t ob, int64_t os, int64_t oh, float* lse_dev,
+                      void* cuda_stream) {
+  return attention_common(in, B, S, H, D, sm_scale, is_causal != 0, out_dev, ob, os, oh, lse_dev, cuda_stream,
+                          launch_attention_tc);
 }
 
 int sage_attention_simt(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
-                        void* out_dev, int64_t ob, int64_t os, int64_t oh, void* cuda_stream) {
-  return attention_common(in, B, S, H, D, sm_scale, out_dev, ob, os, oh, cuda_stream, simt_adapter);
+                        int is_causal, void* out_dev, int64_t ob, int64_t os, int64_t oh, float* lse_dev,
+                        void* cuda_stream) {
+  return attention_common(in, B, S, H, D, sm_scale, is_causal != 0, out_dev, ob, os, oh, lse_dev, cuda_stream,
+                          simt_adapter);
+}
+
+int sage_lse_smooth_k_term(const sage_bf16_tensor* q, const float* k_mean_dev, int64_t B, int64_t S, int64_t H,
+                           int64_t D, float sm_scale, float* lse_dev, void* cuda_stream) {
+  int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  if ((rc = check_bf16_in(q)) != SAGE_OK) return rc;
+  if (k_mean_dev == nullptr || lse_dev == nullptr) return SAGE_ERR_NULLPTR;
+  if (!aligned16(k_mean_dev) || !aligned4(lse_dev)) return SAGE_ERR_ALIGN;
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.0f)) return SAGE_ERR_ARG;
+  int dev = 0;
+  if ((rc = check_device(&dev)) != SAGE_OK) return rc;
+  if (B == 0 || H == 0 || S == 0) return SAGE_OK;
+  const Bf16In qi{static_cast<const uint16_t*>(q->ptr_dev), q->stride_b, q->stride_s, q->stride_h};
+  return cuda_status(launch_lse_smooth_k_term(qi, k_mean_dev, B, S, H, sm_scale, lse_dev,
+                                              static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int sage_sageattn(const void* q_dev, const void* k_dev, const void* v_dev, const int64_t q_shape[4],
@@ -262,57 +368,20 @@ int sage_sageattn(const void* q_dev, const void* k_dev, const void* v_dev, const
   // The contract's rejections come first, in the order the pages list them.
   if (is_causal) return SAGE_ERR_CAUSAL;
   if (return_lse) return SAGE_ERR_LSE;
-  if (q_dtype != SAGE_DTYPE_BF16 || k_dtype != SAGE_DTYPE_BF16 || v_dtype != SAGE_DTYPE_BF16 ||
-      out_dtype != SAGE_DTYPE_BF16)
-    return SAGE_ERR_DTYPE;
-  if (q_shape == nullptr || k_shape == nullptr || v_shape == nullptr || q_strides == nullptr ||
-      k_strides == nullptr || v_strides == nullptr || out_strides == nullptr || tensor_layout == nullptr)
-    return SAGE_ERR_NULLPTR;
-  int is_nhd;
-  if (std::strcmp(tensor_layout, "NHD") == 0) is_nhd = 1;
-  else if (std::strcmp(tensor_layout, "HND") == 0) is_nhd = 0;
-  else return SAGE_ERR_LAYOUT;
-  // axis positions of (b, s, h, d) in the given layout
-  const int ax_s = is_nhd ? 1 : 2, ax_h = is_nhd ? 2 : 1;
-  const int64_t B = q_shape[0], S = q_shape[ax_s], H = q_shape[ax_h], D = q_shape[3];
-  if (D != kHeadDim && D >= 0) return SAGE_ERR_HEAD_DIM;
-  for (int i = 0; i < 4; ++i)
-    if (k_shape[i] != q_shape[i] || v_shape[i] != q_shape[i]) return SAGE_ERR_SHAPE;
-  int rc = check_sizes(B, S, H, D);
-  if (rc != SAGE_OK) return rc;
-  const int64_t* st[4] = {q_strides, k_strides, v_strides, out_strides};
-  for (int i = 0; i < 4; ++i)
-    if (st[i][3] != 1) return SAGE_ERR_LAYOUT;
-  if (!(std::isnan(sm_scale) || (std::isfinite(sm_scale) && sm_scale > 0.0f))) return SAGE_ERR_ARG;
-  const float scale = std::isnan(sm_scale) ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) : sm_scale;
-  const sage_bf16_tensor qt{q_dev, q_strides[0], q_strides[ax_s], q_strides[ax_h]};
-  const sage_bf16_tensor kt{k_dev, k_strides[0], k_strides[ax_s], k_strides[ax_h]};
-  const sage_bf16_tensor vt{v_dev, v_strides[0], v_strides[ax_s], v_strides[ax_h]};
-  if ((rc = check_bf16_in(&qt)) != SAGE_OK || (rc = check_bf16_in(&kt)) != SAGE_OK ||
-      (rc = check_bf16_in(&vt)) != SAGE_OK)
-    return rc;
-  if ((rc = check_out(out_dev, out_strides[0], out_strides[ax_s], out_strides[ax_h])) != SAGE_OK) return rc;
-  if (workspace_dev == nullptr) return SAGE_ERR_NULLPTR;
-  if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return SAGE_ERR_ALIGN;
-  const BundleLayout bl = bundle_layout(B, S, H);
-  const size_t scratch = prologue_scratch_bytes(B, S, H);
-  if (workspace_bytes < bl.total + scratch) return SAGE_ERR_WORKSPACE;
-  int dev = 0;
-  if ((rc = check_device(&dev)) != SAGE_OK) return rc;
-  if (B == 0 || H == 0 || S == 0) return SAGE_OK;
-  const Bundle bundle = carve(workspace_dev, bl);
-  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  const Bf16In qi{static_cast<const uint16_t*>(q_dev), qt.stride_b, qt.stride_s, qt.stride_h};
-  const Bf16In ki{static_cast<const uint16_t*>(k_dev), kt.stride_b, kt.stride_s, kt.stride_h};
-  const Bf16In vi{static_cast<const uint16_t*>(v_dev), vt.stride_b, vt.stride_s, vt.stride_h};
-  // the int8 Q/K codes are not read by the attention kernel, so this path
-  // keeps only their fp16 copies
-  if ((rc = cuda_status(launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, bundle,
-                                        static_cast<char*>(workspace_dev) + bl.total, false, g_err_ptr[dev],
-                                        stream))) != SAGE_OK)
-    return rc;
-  const Out o{static_cast<uint16_t*>(out_dev), out_strides[0], out_strides[ax_s], out_strides[ax_h]};
-  return cuda_status(launch_attention_tc(bundle, B, S, H, scale, o, g_err_ptr[dev], stream));
+  return sageattn_impl(q_dev, k_dev, v_dev, q_shape, k_shape, v_shape, q_strides, k_strides, v_strides, q_dtype,
+                       k_dtype, v_dtype, tensor_layout, false, sm_scale, nullptr, smooth_k, out_dev, out_strides,
+                       out_dtype, workspace_dev, workspace_bytes, cuda_stream);
+}
+
+int sage_sageattn_ex(const void* q_dev, const void* k_dev, const void* v_dev, const int64_t q_shape[4],
+                     const int64_t k_shape[4], const int64_t v_shape[4], const int64_t q_strides[4],
+                     const int64_t k_strides[4], const int64_t v_strides[4], int q_dtype, int k_dtype, int v_dtype,
+                     const char* tensor_layout, int is_causal, float sm_scale, int smooth_k, void* out_dev,
+                     const int64_t out_strides[4], int out_dtype, float* lse_dev, void* workspace_dev,
+                     size_t workspace_bytes, void* cuda_stream) {
+  return sageattn_impl(q_dev, k_dev, v_dev, q_shape, k_shape, v_shape, q_strides, k_strides, v_strides, q_dtype,
+                       k_dtype, v_dtype, tensor_layout, is_causal != 0, sm_scale, lse_dev, smooth_k, out_dev,
+                       out_strides, out_dtype, workspace_dev, workspace_bytes, cuda_stream);
 }
 
 int sage_device_error(void* cuda_stream, int* code) {

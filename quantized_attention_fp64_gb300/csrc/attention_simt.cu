@@ -5,8 +5,9 @@
 // Method: "aiter-sage-attention: SageAttention for AMD RDNA4 (gfx1201)
 // #1222", section "The kernel" (INT8 QK^T, FP8 PV, FP32 accumulation).
 // This kernel exists so tests can cross-check the tensor-core kernel with an
-// independent GPU implementation of the same steps; the library never uses
-// it in place of the tensor-core kernel.
+// independent GPU implementation of the same steps (including the causal mask
+// and the log-sum-exp); the library never uses it in place of the tensor-core
+// kernel.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -31,7 +32,8 @@ __device__ __forceinline__ float2 e4m3x2_decode(uint32_t pair) {
 }
 
 __global__ void __launch_bounds__(kRows, 1) attention_simt_kernel(Bundle in, int64_t S, int64_t S_pad, int64_t H,
-                                                                  float sm_scale, Out out) {
+                                                                  float sm_scale, Out out, int causal,
+                                                                  float* lse) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint32_t* ks = reinterpret_cast<uint32_t*>(smem);                      // [128 keys][32 words]
   float* vs = reinterpret_cast<float*>(smem + kKeyTile * kHeadDim);      // [128 keys][128 dims]
@@ -57,7 +59,9 @@ __global__ void __launch_bounds__(kRows, 1) attention_simt_kernel(Bundle in, int
   for (int d = 0; d < kHeadDim; ++d) acc[d] = 0.0f;
   float m = -INFINITY, l = 0.0f;
 
-  for (int64_t j0 = 0; j0 < S; j0 += kKeyTile) {
+  // with the causal mask, the CTA's rows see the key tiles up to its own
+  const int64_t key_end = causal ? min(S, (static_cast<int64_t>(blockIdx.x) + 1) * kRows) : S;
+  for (int64_t j0 = 0; j0 < key_end; j0 += kKeyTile) {
     __syncthreads();
     {
       const uint4* src = reinterpret_cast<const uint4*>(in.k_codes + (bh * S_pad + j0) * kHeadDim);
@@ -80,7 +84,8 @@ __global__ void __launch_bounds__(kRows, 1) attention_simt_kernel(Bundle in, int
       }
     }
     __syncthreads();
-    const int nk = static_cast<int>(S - j0 < kKeyTile ? S - j0 : kKeyTile);
+    int nk = static_cast<int>(S - j0 < kKeyTile ? S - j0 : kKeyTile);
+    if (causal && row - j0 + 1 < nk) nk = static_cast<int>(row - j0 + 1);  // keys j <= row (at least one)
     // pass 1: tile maximum of the logits
     float tmax = -INFINITY;
     for (int j = 0; j < nk; ++j) {
@@ -111,6 +116,7 @@ __global__ void __launch_bounds__(kRows, 1) attention_simt_kernel(Bundle in, int
     m = m_new;
   }
   if (row >= S) return;
+  if (lse != nullptr) lse[bh * S + row] = m + logf(l);
   const float* sv = in.v_scale + bh * kHeadDim;
   uint16_t* dst = out.p + b * out.sb + row * out.ss + h * out.sh;
 #pragma unroll
@@ -125,14 +131,14 @@ __global__ void __launch_bounds__(kRows, 1) attention_simt_kernel(Bundle in, int
 }  // namespace
 
 cudaError_t launch_attention_simt(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale,
-                                  const Out& out, cudaStream_t stream) {
+                                  const Out& out, bool causal, float* lse, cudaStream_t stream) {
   const int64_t S_pad = padded_len(S);
   const size_t smem = static_cast<size_t>(kKeyTile) * kHeadDim + static_cast<size_t>(kKeyTile) * kHeadDim * 4;
   cudaError_t e = cudaFuncSetAttribute(attention_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(S_pad / kRows), static_cast<unsigned>(H), static_cast<unsigned>(B));
-  attention_simt_kernel<<<grid, kRows, smem, stream>>>(in, S, S_pad, H, sm_scale, out);
+  attention_simt_kernel<<<grid, kRows, smem, stream>>>(in, S, S_pad, H, sm_scale, out, causal ? 1 : 0, lse);
   return cudaGetLastError();
 }
 

@@ -80,9 +80,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLog2P = 8.807354922057604f;    // log2(448)
+constexpr float kLn2 = 0.6931471805599453f;
 
 struct Params {
   int64_t S, S_pad, n_kv, pairs_per_head, n_units;
+  float* lse;  // [B][H][S] natural-log log-sum-exp of each row's logits, or null
   const float* q_scale;
   const float* k_scale;
   const float* v_scale;
@@ -91,6 +93,13 @@ struct Params {
   float sm_log2;  // sm_scale * log2(e)
   int* dev_err;
 };
+
+// Key tiles query tile `qt` reads: all of them, or with the causal mask the
+// tiles up to its diagonal (Q and K have the same length).
+template <bool kCausal>
+__device__ __forceinline__ int64_t key_tiles(const Params& prm, int64_t qt) {
+  return kCausal ? min(prm.n_kv, qt + 1) : prm.n_kv;
+}
 
 struct Ctx {
   uint32_t bar0;
@@ -297,6 +306,9 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& cx, int i, uint32_t tS, 
   return true;
 }
 
+// kCausal: the causal mask (a separate instantiation, so the unmasked kernel
+// carries none of its branches).
+template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params prm) {
@@ -344,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
-  const int64_t n_kv = prm.n_kv;
 
   if (warp < 4) {
     // control warpgroup: one register decrease for all four warps
@@ -371,7 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                               cx.bar(kBarQFull));
           q_pending = static_cast<int>(u_cnt & 1u);
           ++u_cnt;
-          for (int64_t j = 0; ok && j < n_kv; ++j) {
+          // both query tiles' key tiles: those of the second, which sees more
+          const int64_t n_kv_u = key_tiles<kCausal>(prm, 2 * (u % prm.pairs_per_head) + 1);
+          for (int64_t j = 0; ok && j < n_kv_u; ++j) {
             const uint32_t ks = k_cnt % kKStages, kph = (k_cnt / kKStages) & 1u;
             if (!(ok = wait_bar(cx, cx.bar(kBarKEmpty + ks), kph ^ 1u))) break;
             tc::mbar_arrive_expect_tx(cx.bar(kBarKFull + ks), kTile16);
@@ -418,37 +431,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int64_t u = blockIdx.x; ok && u < prm.n_units; u += gridDim.x) {
         if (!(ok = wait_bar_warp(cx, cx.bar(kBarQFull), u_cnt & 1u))) break;
-        for (int64_t j = 0; ok && j <= n_kv; ++j) {
-          if (j < n_kv) {
+        // this tile's key tiles, and the unit's (the ring carries the larger
+        // count; a tile releases the stages it does not use without an MMA)
+        const int64_t qt = 2 * (u % prm.pairs_per_head) + i;
+        const int64_t n_kv_i = key_tiles<kCausal>(prm, qt), n_kv_u = key_tiles<kCausal>(prm, qt | 1);
+        for (int64_t j = 0; ok && j <= n_kv_u; ++j) {
+          if (j < n_kv_u) {
             // QK_j once K_j is loaded and the softmax has read S_{j-1}
             const uint32_t ks = k_cnt % kKStages;
             if (!(ok = wait_bar_warp(cx, cx.bar(kBarKFull + ks), (k_cnt / kKStages) & 1u))) break;
-            if (u_cnt > 0 || j > 0) {
-              if (!(ok = wait_bar_warp(cx, cx.bar(kBarSFree + i), sf_cnt & 1u))) break;
-              ++sf_cnt;
-            }
-            tc::tc_fence_after();
-            if (leader) {
-              issue_qk(d_s, dq, desc_at(dk0, ks * kTile16));
-              tc::mma_commit(cx.bar(kBarSFull + i));
-              tc::mma_commit(cx.bar(kBarKEmpty + ks));
-              if (j == n_kv - 1) tc::mma_commit(cx.bar(kBarQEmpty));
+            if (j < n_kv_i) {
+              if (u_cnt > 0 || j > 0) {
+                if (!(ok = wait_bar_warp(cx, cx.bar(kBarSFree + i), sf_cnt & 1u))) break;
+                ++sf_cnt;
+              }
+              tc::tc_fence_after();
+              if (leader) {
+                issue_qk(d_s, dq, desc_at(dk0, ks * kTile16));
+                tc::mma_commit(cx.bar(kBarSFull + i));
+                tc::mma_commit(cx.bar(kBarKEmpty + ks));
+                if (j == n_kv_i - 1) tc::mma_commit(cx.bar(kBarQEmpty));
+              }
+            } else if (leader) {
+              tc::mbar_arrive(cx.bar(kBarKEmpty + ks));  // masked for this tile
             }
             __syncwarp();
             ++k_cnt;
           }
           if (j >= 1) {
             // PV_{j-1} once P_{j-1} is in shared memory (and O rescaled)
+            const int64_t jj = j - 1;
             const uint32_t vs = v_cnt % kVStages;
             if (!(ok = wait_bar_warp(cx, cx.bar(kBarVFull + vs), (v_cnt / kVStages) & 1u))) break;
-            if (!(ok = wait_bar_warp(cx, cx.bar(kBarPFull + i), p_cnt & 1u))) break;
-            ++p_cnt;
-            if (j == 1 && !(ok = wait_bar_warp(cx, cx.bar(kBarOEmpty + i), (u_cnt & 1u) ^ 1u))) break;
-            tc::tc_fence_after();
-            if (leader) {
-              issue_pv(d_o, dp, desc_at(dv0, vs * kTile8), j > 1);
-              tc::mma_commit(cx.bar(kBarPVDone + i));
-              tc::mma_commit(cx.bar(kBarVEmpty + vs));
+            if (jj < n_kv_i) {
+              if (!(ok = wait_bar_warp(cx, cx.bar(kBarPFull + i), p_cnt & 1u))) break;
+              ++p_cnt;
+              if (jj == 0 && !(ok = wait_bar_warp(cx, cx.bar(kBarOEmpty + i), (u_cnt & 1u) ^ 1u))) break;
+              tc::tc_fence_after();
+              if (leader) {
+                issue_pv(d_o, dp, desc_at(dv0, vs * kTile8), jj > 0);
+                tc::mma_commit(cx.bar(kBarPVDone + i));
+                tc::mma_commit(cx.bar(kBarVEmpty + vs));
+              }
+            } else if (leader) {
+              tc::mbar_arrive(cx.bar(kBarVEmpty + vs));  // masked for this tile
             }
             __syncwarp();
             ++v_cnt;
@@ -489,20 +515,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K scales of a 128-key tile: 4 consecutive floats, 16-byte aligned
       // (S_pad / 32 is a multiple of 4)
       float4 ks_next = __ldg(reinterpret_cast<const float4*>(ks));
-      for (int64_t j = 0; j < n_kv; ++j) {
+      const int64_t qt = 2 * (u % prm.pairs_per_head) + i;  // this query tile
+      const int64_t n_kv_i = key_tiles<kCausal>(prm, qt);
+      for (int64_t j = 0; j < n_kv_i; ++j) {
         cb[0] = cq * ks_next.x;
         cb[1] = cq * ks_next.y;
         cb[2] = cq * ks_next.z;
         cb[3] = cq * ks_next.w;
         // the next tile's scales load while this tile is processed
-        if (j + 1 < n_kv) ks_next = __ldg(reinterpret_cast<const float4*>(ks + (j + 1) * 4));
+        if (j + 1 < n_kv_i) ks_next = __ldg(reinterpret_cast<const float4*>(ks + (j + 1) * 4));
         if (!(ok = wait_bar_warp(cx, cx.bar(kBarSFull + i), s_cnt & 1u))) break;
         ++s_cnt;
         tc::tc_fence_after();
-        const int64_t nvalid = prm.S - j * kKeyTile;  // keys of this tile below S
-        ok = nvalid >= kKeyTile
+        // keys of this tile the row may see: those below S and, on the
+        // diagonal tile of the causal mask, those at or before the row. The
+        // choice of path must be the same in every lane (the tile code is
+        // warp-collective), so a tile with any limit takes the masked path
+        // in all lanes, each with its own limit.
+        const int64_t below_s = prm.S - j * kKeyTile;
+        const bool diagonal = kCausal && j == qt;
+        int64_t lim = below_s < kKeyTile ? below_s : kKeyTile;
+        if (diagonal && lim > row + 1) lim = row + 1;
+        ok = !(diagonal || below_s < kKeyTile)
                  ? softmax_tile<false>(cx, i, tS, tO, p_row, row, cb, kKeyTile, j == 0, pv_cnt, m, l)
-                 : softmax_tile<true>(cx, i, tS, tO, p_row, row, cb, static_cast<int>(nvalid), j == 0, pv_cnt, m, l);
+                 : softmax_tile<true>(cx, i, tS, tO, p_row, row, cb, static_cast<int>(lim), j == 0, pv_cnt, m, l);
         if (!ok) break;
         tc::tc_fence_before();
         tc::mbar_arrive(cx.bar(kBarPFull + i));
@@ -514,6 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++pv_cnt;
       tc::tc_fence_after();
       const float inv_l = 1.0f / l;
+      if (prm.lse != nullptr && row_valid) {
+        // ln(sum_j e^logit) = (m + log2(l) - log2(448)) * ln 2, m and the
+        // logits in base 2, l counting 448 * 2^(x - m)
+        prm.lse[bh * prm.S + qrow] = (m + log2f(l) - kLog2P) * kLn2;
+      }
       const float* sv = prm.v_scale + bh * kHeadDim;
       const int64_t b_idx = bh / prm.H, h_idx = bh % prm.H;
       uint16_t* dst = prm.out.p + b_idx * prm.out.sb + qrow * prm.out.ss + h_idx * prm.out.sh;
@@ -564,7 +605,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void
 }  // namespace
 
 cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale, const Out& out,
-                                int* dev_err, cudaStream_t stream) {
+                                bool causal, float* lse, int* dev_err, cudaStream_t stream) {
   const int64_t S_pad = padded_len(S);
   const int64_t BH = B * H;
   CUtensorMap tq, tk, tv;
@@ -587,13 +628,15 @@ cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t 
   p.out = out;
   p.H = H;
   p.sm_log2 = sm_scale * kLog2e;
+  p.lse = lse;
   p.dev_err = dev_err;
-  cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kernel = causal ? attention_tc_kernel<true> : attention_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int sms = sm_count_current();
   const int grid = static_cast<int>(p.n_units < sms ? p.n_units : sms);
-  attention_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -66,9 +66,17 @@ int* device_error_ptr();
 size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H);
 
 cudaError_t launch_attention_simt(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale,
-                                  const Out& out, cudaStream_t stream);
+                                  const Out& out, bool causal, float* lse, cudaStream_t stream);
 
+// causal: query i sees keys j <= i only. lse: null, or [B][H][S] fp32 that
+// receives each row's natural-log log-sum-exp of its logits (of the keys the
+// bundle holds, i.e. of k - mean when it was quantized with smooth_k).
 cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale,
-                                const Out& out, int* dev_err, cudaStream_t stream);
+                                const Out& out, bool causal, float* lse, int* dev_err, cudaStream_t stream);
+
+// Adds sm_scale * q_i . k_mean to lse[b][h][i] (the smooth_k term that turns
+// the log-sum-exp of the mean-reduced keys into that of the original keys).
+cudaError_t launch_lse_smooth_k_term(const Bf16In& q, const float* k_mean, int64_t B, int64_t S, int64_t H,
+                                     float sm_scale, float* lse, cudaStream_t stream);
 
 }  // namespace sage

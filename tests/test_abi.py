@@ -126,8 +126,10 @@ def test_quantize_and_attention_rejections(lib):
     qz_bad = _lib.Quantized(0x100000, 0x200004, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000, 0x800000,
                             0x900000)
     out = ctypes.c_void_p(0x900000)
-    for fn in ("sage_attention", "sage_attention_simt"):
-        f = getattr(lib, fn)
+    plain = lib.sage_attention
+    ex = [lambda *a, fn=fn: getattr(lib, fn)(*a[:6], 1, *a[6:10], None, a[10])
+          for fn in ("sage_attention_ex", "sage_attention_simt")]
+    for f in [plain] + ex:
         assert f(r(qz), 1, 256, 2, 128, ctypes.c_float(-0.1), out, 65536, 256, 128, None) == ARG
         assert f(r(qz), 1, 256, 2, 128, ctypes.c_float(math.nan), out, 65536, 256, 128, None) == ARG
         assert f(r(qz_bad), 1, 256, 2, 128, ctypes.c_float(0.1), out, 65536, 256, 128, None) == ALIGN
@@ -135,6 +137,16 @@ def test_quantize_and_attention_rejections(lib):
         assert f(None, 1, 256, 2, 128, ctypes.c_float(0.1), out, 65536, 256, 128, None) == NULLPTR
         assert f(r(qz), 1, 256, 2, 128, ctypes.c_float(0.1), None, 65536, 256, 128, None) == NULLPTR
         assert f(r(qz), 1, 256, 2, 128, ctypes.c_float(0.1), out, 65536, 252, 128, None) == ALIGN
+    # a misaligned log-sum-exp buffer
+    for fn in ("sage_attention_ex", "sage_attention_simt"):
+        assert getattr(lib, fn)(r(qz), 1, 256, 2, 128, ctypes.c_float(0.1), 1, out, 65536, 256, 128,
+                                ctypes.c_void_p(0xA00002), None) == ALIGN
+    assert lib.sage_lse_smooth_k_term(r(t), ctypes.c_void_p(0x700000), 1, 256, 2, 128, ctypes.c_float(0.1),
+                                      ctypes.c_void_p(0xA00002), None) == ALIGN
+    assert lib.sage_lse_smooth_k_term(r(t), None, 1, 256, 2, 128, ctypes.c_float(0.1),
+                                      ctypes.c_void_p(0xA00000), None) == NULLPTR
+    assert lib.sage_lse_smooth_k_term(r(t), ctypes.c_void_p(0x700000), 1, 256, 2, 64, ctypes.c_float(0.1),
+                                      ctypes.c_void_p(0xA00000), None) == HEAD_DIM
 
 
 def test_python_binding_rejects_host_tensors():
@@ -142,3 +154,31 @@ def test_python_binding_rejects_host_tensors():
     with pytest.raises(ValueError):
         sageattn(q, q, q)
     assert issubclass(SageError, ValueError)
+
+
+def _call_sageattn_ex(lib, lse_ptr=0x60000, **over):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, shape=(1, 256, 2, 128), kshape=None, vshape=None,
+             strides=(256 * 2 * 128, 2 * 128, 128, 1), dt=0, kdt=0, vdt=0, layout=b"NHD", causal=1, sm=float("nan"),
+             smooth=1, out=0x40000, ostrides=None, odt=0, ws=0x50000, wsn=1 << 40)
+    a.update(over)
+    I = _lib.I64x4
+    return lib.sage_sageattn_ex(ctypes.c_void_p(a["q"]), ctypes.c_void_p(a["k"]), ctypes.c_void_p(a["v"]),
+                                I(*a["shape"]), I(*(a["kshape"] or a["shape"])), I(*(a["vshape"] or a["shape"])),
+                                I(*a["strides"]), I(*a["strides"]), I(*a["strides"]), a["dt"], a["kdt"], a["vdt"],
+                                a["layout"], a["causal"], ctypes.c_float(a["sm"]), a["smooth"],
+                                ctypes.c_void_p(a["out"]), I(*(a["ostrides"] or a["strides"])), a["odt"],
+                                ctypes.c_void_p(lse_ptr), ctypes.c_void_p(a["ws"]), a["wsn"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dt=1), DTYPE), (dict(odt=1), DTYPE),
+    (dict(shape=(1, 256, 2, 64)), HEAD_DIM),
+    (dict(kshape=(1, 255, 2, 128)), SHAPE),
+    (dict(layout=b"BSHD"), LAYOUT),
+    (dict(out=0x40004), ALIGN), (dict(lse_ptr=0x60002), ALIGN),
+    (dict(ws=0), NULLPTR), (dict(wsn=1000), WORKSPACE), (dict(sm=-1.0), ARG),
+])
+def test_sageattn_ex_keeps_the_other_checks(lib, over, code):
+    # the extended entry honours is_causal and the log-sum-exp (here both on)
+    # and still rejects everything else sage_sageattn rejects
+    assert _call_sageattn_ex(lib, **over) == code
