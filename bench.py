@@ -319,6 +319,10 @@ def run_gpu(args):
 
     t_pro = graph_time(lambda: quantize(q, k, v, "NHD", True, out=qz, scratch=scratch))
     t_att = graph_time(lambda: attention(qz, sm, out=out))
+    # the causal mask (sage_attention_ex): the kernel skips the key tiles a
+    # query tile cannot see, so it does the visible half of the work
+    t_att_causal = graph_time(lambda: attention(qz, sm, out=out, is_causal=True))
+    ops_causal = 4.0 * B * H * D * (S * (S + 1) / 2)
     if device_error() != 0:
         raise RuntimeError("device error word set during timing")
 
@@ -377,6 +381,9 @@ def run_gpu(args):
                      "peak_note": f"harmonic mean of fp16 {p16:.1f} and e4m3 {p8:.1f} TFLOP/s "
                                   f"({peak_kind} bf16 burst: the kernel is timed alone; e4m3 = 2x nominal ratio)"},
         "attention_kernel": {"ms": t_att * 1e3, "tflops": att_tflops, "frac_of_peak": att_tflops / p_att},
+        "attention_kernel_causal": {"ms": t_att_causal * 1e3, "visible_ops": ops_causal,
+                                    "tflops": ops_causal / t_att_causal / 1e12,
+                                    "frac_of_peak": ops_causal / t_att_causal / 1e12 / p_att},
         "prologue": {"ms": t_pro * 1e3, "call": "sage_quantize", "algorithmic_bytes": pro_bytes,
                      "gbs": pro_bytes / t_pro / 1e9, "frac_of_hbm": pro_bytes / t_pro / 1e9 / peaks["hbm_gbs"],
                      "bytes_written_and_read": pro_moved, "gbs_moved": pro_moved / t_pro / 1e9,
