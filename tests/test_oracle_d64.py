@@ -46,7 +46,8 @@ def test_int8_blocks_bruteforce_d64():
                 q = float(np.float32(blk[r, c] / scales[t]))   # fl32(x / s)
                 assert codes[32 * t + r, c] == round(q)        # round half even (Python round)
                 # within half a step, up to the rounding of the quotient x / s
-                assert abs(Fraction(float(blk[r, c])) - codes[32 * t + r, c] * s) <= s / 2 * (1 + Fraction(1, 2 ** 20))
+                # (fl32(x / s) is within half an ulp of 127.5 or less: 2^-18)
+                assert abs(Fraction(float(blk[r, c])) - codes[32 * t + r, c] * s) <= s * (Fraction(1, 2) + Fraction(1, 2 ** 17))
 
 
 def test_key_mean_d64_matches_fsum():
