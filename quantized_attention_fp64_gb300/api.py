@@ -73,18 +73,19 @@ class QuantizedQKV:
     """Quantized bundle (views into one device buffer, see sage_quantized)."""
 
     buffer: torch.Tensor
-    q_codes: torch.Tensor   # int8 [B, H, S_pad, 128]
-    k_codes: torch.Tensor   # int8 [B, H, S_pad, 128]
-    vt_codes: torch.Tensor  # uint8 (e4m3fn) [B, H, 128, S_pad]
+    q_codes: torch.Tensor   # int8 [B, H, S_pad, D]
+    k_codes: torch.Tensor   # int8 [B, H, S_pad, D]
+    vt_codes: torch.Tensor  # uint8 (e4m3fn) [B, H, D, S_pad]
     q_scale: torch.Tensor   # float32 [B, H, S_pad/32]
     k_scale: torch.Tensor   # float32 [B, H, S_pad/32]
-    v_scale: torch.Tensor   # float32 [B, H, 128]
-    k_mean: torch.Tensor    # float32 [B, H, 128]
-    q16: torch.Tensor       # float16 [B, H, S_pad, 128], the Q codes as fp16 values
-    k16: torch.Tensor       # float16 [B, H, S_pad, 128], the K codes as fp16 values
+    v_scale: torch.Tensor   # float32 [B, H, D]
+    k_mean: torch.Tensor    # float32 [B, H, D]
+    q16: torch.Tensor       # float16 [B, H, S_pad, D], the Q codes as fp16 values
+    k16: torch.Tensor       # float16 [B, H, S_pad, D], the K codes as fp16 values
     B: int
     S: int
     H: int
+    D: int = 128
 
     def c_struct(self) -> _lib.Quantized:
         return _lib.Quantized(*(t.data_ptr() for t in (self.q_codes, self.k_codes, self.vt_codes, self.q_scale,
@@ -92,13 +93,13 @@ class QuantizedQKV:
                                                        self.k16)))
 
 
-def alloc_bundle(B: int, S: int, H: int, device) -> QuantizedQKV:
+def alloc_bundle(B: int, S: int, H: int, device, D: int = 128) -> QuantizedQKV:
     lib = _lib.load()
     n = ctypes.c_size_t(0)
-    _check(lib.sage_bundle_size(B, S, H, 128, ctypes.byref(n), None, None))
+    _check(lib.sage_bundle_size(B, S, H, D, ctypes.byref(n), None, None))
     buf = torch.empty(max(n.value, 256), dtype=torch.uint8, device=device)
     c = _lib.Quantized()
-    _check(lib.sage_bundle_size(B, S, H, 128, ctypes.byref(n), ctypes.c_void_p(buf.data_ptr()), ctypes.byref(c)))
+    _check(lib.sage_bundle_size(B, S, H, D, ctypes.byref(n), ctypes.c_void_p(buf.data_ptr()), ctypes.byref(c)))
     s_pad = -(-S // 128) * 128
     base = buf.data_ptr()
 
@@ -112,16 +113,16 @@ def alloc_bundle(B: int, S: int, H: int, device) -> QuantizedQKV:
 
     return QuantizedQKV(
         buffer=buf,
-        q_codes=view(c.q_codes_dev, torch.int8, (B, H, s_pad, 128)),
-        k_codes=view(c.k_codes_dev, torch.int8, (B, H, s_pad, 128)),
-        vt_codes=view(c.vt_codes_dev, torch.uint8, (B, H, 128, s_pad)),
+        q_codes=view(c.q_codes_dev, torch.int8, (B, H, s_pad, D)),
+        k_codes=view(c.k_codes_dev, torch.int8, (B, H, s_pad, D)),
+        vt_codes=view(c.vt_codes_dev, torch.uint8, (B, H, D, s_pad)),
         q_scale=view(c.q_scale_dev, torch.float32, (B, H, s_pad // 32)),
         k_scale=view(c.k_scale_dev, torch.float32, (B, H, s_pad // 32)),
-        v_scale=view(c.v_scale_dev, torch.float32, (B, H, 128)),
-        k_mean=view(c.k_mean_dev, torch.float32, (B, H, 128)),
-        q16=view(c.q16_dev, torch.float16, (B, H, s_pad, 128)),
-        k16=view(c.k16_dev, torch.float16, (B, H, s_pad, 128)),
-        B=B, S=S, H=H)
+        v_scale=view(c.v_scale_dev, torch.float32, (B, H, D)),
+        k_mean=view(c.k_mean_dev, torch.float32, (B, H, D)),
+        q16=view(c.q16_dev, torch.float16, (B, H, s_pad, D)),
+        k16=view(c.k16_dev, torch.float16, (B, H, s_pad, D)),
+        B=B, S=S, H=H, D=D)
 
 
 def _bf16_tensor(t: torch.Tensor, layout: str) -> _lib.Bf16Tensor:
@@ -152,7 +153,7 @@ def quantize(q, k, v, tensor_layout: str = "NHD", smooth_k: bool = True, out: Qu
         raise SageError(-3, "inputs and output must be bfloat16")
     lib = _lib.load()
     with torch.cuda.device(q.device):
-        qz = out if out is not None else alloc_bundle(B, S, H, q.device)
+        qz = out if out is not None else alloc_bundle(B, S, H, q.device, D)
         if scratch is None:
             scratch = torch.empty(max(quantize_scratch_size(B, S, H, D), 256), dtype=torch.uint8, device=q.device)
         bundle = qz.c_struct()
@@ -166,21 +167,21 @@ def quantize(q, k, v, tensor_layout: str = "NHD", smooth_k: bool = True, out: Qu
 def _attention(fn_name: str, qz: QuantizedQKV, sm_scale, tensor_layout: str, out, is_causal=False,
                return_lse=False):
     lib = _lib.load()
-    B, S, H = qz.B, qz.S, qz.H
+    B, S, H, D = qz.B, qz.S, qz.H, qz.D
     device = qz.buffer.device
     if out is None:
-        shape = (B, H, S, 128) if tensor_layout == "HND" else (B, S, H, 128)
+        shape = (B, H, S, D) if tensor_layout == "HND" else (B, S, H, D)
         out = torch.empty(shape, dtype=torch.bfloat16, device=device)
-    scale = (1.0 / math.sqrt(128.0)) if sm_scale is None else float(sm_scale)
+    scale = (1.0 / math.sqrt(D)) if sm_scale is None else float(sm_scale)
     ob, os_, oh = _bsh_strides(out, tensor_layout)
     bundle = qz.c_struct()
     lse = torch.empty((B, H, S), dtype=torch.float32, device=device) if return_lse else None
     with torch.cuda.device(device):
         if fn_name == "sage_attention":
-            _check(lib.sage_attention(ctypes.byref(bundle), B, S, H, 128, ctypes.c_float(scale),
+            _check(lib.sage_attention(ctypes.byref(bundle), B, S, H, D, ctypes.c_float(scale),
                                       ctypes.c_void_p(out.data_ptr()), ob, os_, oh, _stream(device)))
         else:
-            _check(getattr(lib, fn_name)(ctypes.byref(bundle), B, S, H, 128, ctypes.c_float(scale),
+            _check(getattr(lib, fn_name)(ctypes.byref(bundle), B, S, H, D, ctypes.c_float(scale),
                                          int(bool(is_causal)), ctypes.c_void_p(out.data_ptr()), ob, os_, oh,
                                          ctypes.c_void_p(lse.data_ptr() if lse is not None else None),
                                          _stream(device)))
@@ -210,10 +211,10 @@ def lse_smooth_k_term(q: torch.Tensor, qz: QuantizedQKV, lse: torch.Tensor, sm_s
     the log-sum-exp of the mean-reduced keys becomes that of the original keys."""
     _require_cuda(q)
     lib = _lib.load()
-    scale = (1.0 / math.sqrt(128.0)) if sm_scale is None else float(sm_scale)
+    scale = (1.0 / math.sqrt(qz.D)) if sm_scale is None else float(sm_scale)
     with torch.cuda.device(q.device):
         _check(lib.sage_lse_smooth_k_term(ctypes.byref(_bf16_tensor(q, tensor_layout)),
-                                          ctypes.c_void_p(qz.k_mean.data_ptr()), qz.B, qz.S, qz.H, 128,
+                                          ctypes.c_void_p(qz.k_mean.data_ptr()), qz.B, qz.S, qz.H, qz.D,
                                           ctypes.c_float(scale), ctypes.c_void_p(lse.data_ptr()), _stream(q.device)))
     return lse
 

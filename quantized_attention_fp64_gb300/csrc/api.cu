@@ -55,10 +55,10 @@ int check_device(int* dev_out) {
 
 int check_sizes(int64_t B, int64_t S, int64_t H, int64_t D) {
   if (B < 0 || S < 0 || H < 0 || D < 0) return SAGE_ERR_SHAPE;
-  if (D != kHeadDim) return SAGE_ERR_HEAD_DIM;
+  if (D != kHeadDim && D != 64) return SAGE_ERR_HEAD_DIM;
   if (B > kMaxBH || H > kMaxBH || S > kMaxS) return SAGE_ERR_TOO_LARGE;
   if (B * H > kMaxBH * 16) return SAGE_ERR_TOO_LARGE;
-  if (B * H * padded_len(S) > kMaxElems / kHeadDim) return SAGE_ERR_TOO_LARGE;
+  if (B * H * padded_len(S) > kMaxElems / D) return SAGE_ERR_TOO_LARGE;
   return SAGE_OK;
 }
 
@@ -74,12 +74,13 @@ struct BundleLayout {
   size_t total;
 };
 
-BundleLayout bundle_layout(int64_t B, int64_t S, int64_t H) {
+BundleLayout bundle_layout(int64_t B, int64_t S, int64_t H, int64_t D) {
   const size_t bh = static_cast<size_t>(B * H);
   const size_t sp = static_cast<size_t>(padded_len(S));
-  const size_t sizes[kBundleArrays] = {bh * sp * kHeadDim,         bh * sp * kHeadDim,         bh * sp * kHeadDim,
-                                       bh * (sp / kQKBlock) * 4,   bh * (sp / kQKBlock) * 4,   bh * kHeadDim * 4,
-                                       bh * kHeadDim * 4,          bh * sp * kHeadDim * 2,     bh * sp * kHeadDim * 2};
+  const size_t d = static_cast<size_t>(D);
+  const size_t sizes[kBundleArrays] = {bh * sp * d,                bh * sp * d,                bh * sp * d,
+                                       bh * (sp / kQKBlock) * 4,   bh * (sp / kQKBlock) * 4,   bh * d * 4,
+                                       bh * d * 4,                 bh * sp * d * 2,            bh * sp * d * 2};
   BundleLayout l;
   size_t o = 0;
   for (int i = 0; i < kBundleArrays; ++i) {
@@ -147,11 +148,11 @@ int check_out(const void* out, int64_t ob, int64_t os, int64_t oh) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA; }
 
-typedef cudaError_t (*AttnLaunch)(const Bundle&, int64_t, int64_t, int64_t, float, const Out&, bool, float*, int*,
-                                  cudaStream_t);
+typedef cudaError_t (*AttnLaunch)(const Bundle&, int64_t, int64_t, int64_t, int64_t, float, const Out&, bool,
+                                  float*, int*, cudaStream_t);
 
-cudaError_t simt_adapter(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm, const Out& o, bool causal,
-                         float* lse, int*, cudaStream_t st) {
+cudaError_t simt_adapter(const Bundle& in, int64_t B, int64_t S, int64_t H, int64_t, float sm, const Out& o,
+                         bool causal, float* lse, int*, cudaStream_t st) {
   return launch_attention_simt(in, B, S, H, sm, o, causal, lse, st);
 }
 
@@ -170,7 +171,7 @@ int attention_common(const sage_quantized* in, int64_t B, int64_t S, int64_t H, 
   if ((rc = check_device(&dev)) != SAGE_OK) return rc;
   if (B == 0 || H == 0 || S == 0) return SAGE_OK;
   Out o{static_cast<uint16_t*>(out_dev), ob, os, oh};
-  return cuda_status(launch(to_bundle(in), B, S, H, sm_scale, o, causal, lse_dev, g_err_ptr[dev],
+  return cuda_status(launch(to_bundle(in), B, S, H, D, sm_scale, o, causal, lse_dev, g_err_ptr[dev],
                             static_cast<cudaStream_t>(stream)));
 }
 
@@ -209,7 +210,7 @@ int sageattn_impl(const void* q_dev, const void* k_dev, const void* v_dev, const
   // axis positions of (b, s, h, d) in the given layout
   const int ax_s = is_nhd ? 1 : 2, ax_h = is_nhd ? 2 : 1;
   const int64_t B = q_shape[0], S = q_shape[ax_s], H = q_shape[ax_h], D = q_shape[3];
-  if (D != kHeadDim && D >= 0) return SAGE_ERR_HEAD_DIM;
+  if (D != kHeadDim && D != 64 && D >= 0) return SAGE_ERR_HEAD_DIM;
   for (int i = 0; i < 4; ++i)
     if (k_shape[i] != q_shape[i] || v_shape[i] != q_shape[i]) return SAGE_ERR_SHAPE;
   int rc = check_sizes(B, S, H, D);
@@ -229,8 +230,8 @@ int sageattn_impl(const void* q_dev, const void* k_dev, const void* v_dev, const
   if (lse_dev != nullptr && !aligned4(lse_dev)) return SAGE_ERR_ALIGN;
   if (workspace_dev == nullptr) return SAGE_ERR_NULLPTR;
   if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return SAGE_ERR_ALIGN;
-  const BundleLayout bl = bundle_layout(B, S, H);
-  const size_t scratch = prologue_scratch_bytes(B, S, H);
+  const BundleLayout bl = bundle_layout(B, S, H, D);
+  const size_t scratch = prologue_scratch_bytes(B, S, H, D);
   if (workspace_bytes < bl.total + scratch) return SAGE_ERR_WORKSPACE;
   int dev = 0;
   if ((rc = check_device(&dev)) != SAGE_OK) return rc;
@@ -242,16 +243,16 @@ int sageattn_impl(const void* q_dev, const void* k_dev, const void* v_dev, const
   const Bf16In vi{static_cast<const uint16_t*>(v_dev), vt.stride_b, vt.stride_s, vt.stride_h};
   // the int8 Q/K codes are not read by the attention kernel, so this path
   // keeps only their fp16 copies
-  if ((rc = cuda_status(launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, bundle,
+  if ((rc = cuda_status(launch_prologue(qi, ki, vi, B, S, H, D, smooth_k != 0, bundle,
                                         static_cast<char*>(workspace_dev) + bl.total, false, g_err_ptr[dev],
                                         stream))) != SAGE_OK)
     return rc;
   const Out o{static_cast<uint16_t*>(out_dev), out_strides[0], out_strides[ax_s], out_strides[ax_h]};
-  if ((rc = cuda_status(launch_attention_tc(bundle, B, S, H, scale, o, causal, lse_dev, g_err_ptr[dev], stream))) !=
+  if ((rc = cuda_status(launch_attention_tc(bundle, B, S, H, D, scale, o, causal, lse_dev, g_err_ptr[dev], stream))) !=
       SAGE_OK)
     return rc;
   if (lse_dev != nullptr && smooth_k != 0)
-    return cuda_status(launch_lse_smooth_k_term(qi, bundle.k_mean, B, S, H, scale, lse_dev, stream));
+    return cuda_status(launch_lse_smooth_k_term(qi, bundle.k_mean, B, S, H, D, scale, lse_dev, stream));
   return SAGE_OK;
 }
 
@@ -267,7 +268,7 @@ int sage_bundle_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes, 
   if (bytes == nullptr) return SAGE_ERR_NULLPTR;
   const int rc = check_sizes(B, S, H, D);
   if (rc != SAGE_OK) return rc;
-  const BundleLayout l = bundle_layout(B, S, H);
+  const BundleLayout l = bundle_layout(B, S, H, D);
   *bytes = l.total;
   if (base_dev != nullptr) {
     if (bundle == nullptr) return SAGE_ERR_NULLPTR;
@@ -290,7 +291,7 @@ int sage_quantize_scratch_size(int64_t B, int64_t S, int64_t H, int64_t D, size_
   if (bytes == nullptr) return SAGE_ERR_NULLPTR;
   const int rc = check_sizes(B, S, H, D);
   if (rc != SAGE_OK) return rc;
-  *bytes = prologue_scratch_bytes(B, S, H);
+  *bytes = prologue_scratch_bytes(B, S, H, D);
   return SAGE_OK;
 }
 
@@ -298,7 +299,7 @@ int sage_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* byte
   if (bytes == nullptr) return SAGE_ERR_NULLPTR;
   const int rc = check_sizes(B, S, H, D);
   if (rc != SAGE_OK) return rc;
-  *bytes = bundle_layout(B, S, H).total + prologue_scratch_bytes(B, S, H);
+  *bytes = bundle_layout(B, S, H, D).total + prologue_scratch_bytes(B, S, H, D);
   return SAGE_OK;
 }
 
@@ -312,14 +313,14 @@ int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k, const sa
   if ((rc = check_bundle(out, true)) != SAGE_OK) return rc;
   if (scratch_dev == nullptr) return SAGE_ERR_NULLPTR;
   if ((reinterpret_cast<uintptr_t>(scratch_dev) & 255u) != 0) return SAGE_ERR_ALIGN;
-  if (scratch_bytes < prologue_scratch_bytes(B, S, H)) return SAGE_ERR_WORKSPACE;
+  if (scratch_bytes < prologue_scratch_bytes(B, S, H, D)) return SAGE_ERR_WORKSPACE;
   int dev = 0;
   if ((rc = check_device(&dev)) != SAGE_OK) return rc;
   if (B == 0 || H == 0 || S == 0) return SAGE_OK;
   const Bf16In qi{static_cast<const uint16_t*>(q->ptr_dev), q->stride_b, q->stride_s, q->stride_h};
   const Bf16In ki{static_cast<const uint16_t*>(k->ptr_dev), k->stride_b, k->stride_s, k->stride_h};
   const Bf16In vi{static_cast<const uint16_t*>(v->ptr_dev), v->stride_b, v->stride_s, v->stride_h};
-  return cuda_status(launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, to_bundle(out), scratch_dev, true,
+  return cuda_status(launch_prologue(qi, ki, vi, B, S, H, D, smooth_k != 0, to_bundle(out), scratch_dev, true,
                                      g_err_ptr[dev], static_cast<cudaStream_t>(cuda_stream)));
 }
 
@@ -339,6 +340,7 @@ int sage_attention_ex(const sage_quantized* in, int64_t B, int64_t S, int64_t H,
 int sage_attention_simt(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
                         int is_causal, void* out_dev, int64_t ob, int64_t os, int64_t oh, float* lse_dev,
                         void* cuda_stream) {
+  if (D != kHeadDim) return SAGE_ERR_HEAD_DIM;  // the cross-check kernel is written for 128 channels
   return attention_common(in, B, S, H, D, sm_scale, is_causal != 0, out_dev, ob, os, oh, lse_dev, cuda_stream,
                           simt_adapter);
 }
@@ -355,7 +357,7 @@ int sage_lse_smooth_k_term(const sage_bf16_tensor* q, const float* k_mean_dev, i
   if ((rc = check_device(&dev)) != SAGE_OK) return rc;
   if (B == 0 || H == 0 || S == 0) return SAGE_OK;
   const Bf16In qi{static_cast<const uint16_t*>(q->ptr_dev), q->stride_b, q->stride_s, q->stride_h};
-  return cuda_status(launch_lse_smooth_k_term(qi, k_mean_dev, B, S, H, sm_scale, lse_dev,
+  return cuda_status(launch_lse_smooth_k_term(qi, k_mean_dev, B, S, H, D, sm_scale, lse_dev,
                                               static_cast<cudaStream_t>(cuda_stream)));
 }
 
@@ -368,6 +370,9 @@ int sage_sageattn(const void* q_dev, const void* k_dev, const void* v_dev, const
   // The contract's rejections come first, in the order the pages list them.
   if (is_causal) return SAGE_ERR_CAUSAL;
   if (return_lse) return SAGE_ERR_LSE;
+  if (q_dtype == SAGE_DTYPE_BF16 && k_dtype == SAGE_DTYPE_BF16 && v_dtype == SAGE_DTYPE_BF16 &&
+      out_dtype == SAGE_DTYPE_BF16 && q_shape != nullptr && q_shape[3] != kHeadDim && q_shape[3] >= 0)
+    return SAGE_ERR_HEAD_DIM;
   return sageattn_impl(q_dev, k_dev, v_dev, q_shape, k_shape, v_shape, q_strides, k_strides, v_strides, q_dtype,
                        k_dtype, v_dtype, tensor_layout, false, sm_scale, nullptr, smooth_k, out_dev, out_strides,
                        out_dtype, workspace_dev, workspace_bytes, cuda_stream);

@@ -50,16 +50,20 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kKStages = 2;
 constexpr int kVStages = 3;
-constexpr uint32_t kTile8 = 128 * 128;       // bytes of one e4m3 tile
-constexpr uint32_t kTile16 = 128 * 128 * 2;  // bytes of one fp16 tile (two 64-channel subtiles)
-constexpr uint32_t kSub16 = 128 * 128;       // bytes of one 64-channel fp16 subtile
+constexpr uint32_t kTile8 = 128 * 128;       // bytes of one e4m3 P tile (128 rows x 128 keys)
+constexpr uint32_t kSub16 = 128 * 128;       // bytes of one 64-channel fp16 subtile (128 rows)
 
-// shared memory layout (offsets from a 1024-aligned base)
-constexpr uint32_t kOffQ16 = 0;                          // 2 query tiles
-constexpr uint32_t kOffK16 = kOffQ16 + 2 * kTile16;      // K ring
-constexpr uint32_t kOffV = kOffK16 + kKStages * kTile16; // V ring
-constexpr uint32_t kOffP = kOffV + kVStages * kTile8;    // 2 P tiles
-constexpr uint32_t kOffBar = kOffP + 2 * kTile8;
+// Shared memory layout for head dimension D (offsets from a 1024-aligned base).
+template <int D>
+struct Smem {
+  static constexpr uint32_t kTile16 = 128 * D * 2;                     // fp16 Q or K tile: D / 64 subtiles
+  static constexpr uint32_t kTileV = D * 128;                          // e4m3 V^T tile: D rows of 128 keys
+  static constexpr uint32_t kOffQ16 = 0;                               // 2 query tiles
+  static constexpr uint32_t kOffK16 = kOffQ16 + 2 * kTile16;           // K ring
+  static constexpr uint32_t kOffV = kOffK16 + kKStages * kTile16;      // V ring
+  static constexpr uint32_t kOffP = kOffV + kVStages * kTileV;         // 2 P tiles
+  static constexpr uint32_t kOffBar = kOffP + 2 * kTile8;
+};
 // barriers (8 bytes each)
 constexpr int kBarQFull = 0, kBarQEmpty = 1;
 constexpr int kBarKFull = 2, kBarKEmpty = kBarKFull + kKStages;
@@ -68,13 +72,17 @@ constexpr int kBarSFull = kBarVEmpty + kVStages, kBarSFree = kBarSFull + 2;
 constexpr int kBarPFull = kBarSFree + 2, kBarPVDone = kBarPFull + 2;
 constexpr int kBarOEmpty = kBarPVDone + 2, kBarDrain = kBarOEmpty + 2;
 constexpr int kNumBars = kBarDrain + 2;
-constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr uint32_t kOffAbort = kOffTmemSlot + 8;
-constexpr uint32_t kSmemBytes = kOffAbort + 8 + 1024;  // + alignment slack
+template <int D>
+struct SmemTail {
+  static constexpr uint32_t kOffTmemSlot = Smem<D>::kOffBar + kNumBars * 8;
+  static constexpr uint32_t kOffAbort = kOffTmemSlot + 8;
+  static constexpr uint32_t kBytes = kOffAbort + 8 + 1024;  // + alignment slack
+};
 
-// TMEM columns: S of query tile i at 128*i, O of query tile i at 256 + 128*i
+// TMEM columns: S of query tile i at 128*i, O of query tile i (D columns) at 256 + D*i
 __host__ __device__ constexpr uint32_t col_s(int i) { return 128u * static_cast<uint32_t>(i); }
-__host__ __device__ constexpr uint32_t col_o(int i) { return 256u + 128u * static_cast<uint32_t>(i); }
+template <int D>
+__host__ __device__ constexpr uint32_t col_o(int i) { return 256u + static_cast<uint32_t>(D) * static_cast<uint32_t>(i); }
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
@@ -178,24 +186,27 @@ __device__ __forceinline__ void regs_inc() {
 // (offset >> 4) with no carry out of the field.
 __device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t offset) { return base + (offset >> 4); }
 
-// S_i = Q_i K^T for one 128-key tile: 8 MMAs of K = 16 over the two
+// S_i = Q_i K^T for one 128-key tile: D / 16 MMAs of K = 16 over the
 // 64-channel subtiles of the fp16 Q and K tiles (dq, dk: descriptors of the
 // two tiles' first subtiles).
+template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
+  for (int ks = 0; ks < D / 16; ++ks) {
     const uint32_t off = static_cast<uint32_t>(ks >> 2) * kSub16 + static_cast<uint32_t>(ks & 3) * 32u;
     tc::mma_f16_ss(d_tmem, desc_at(dq, off), desc_at(dk, off), tc::kIdescM128N128, ks > 0 ? 1u : 0u);
   }
 }
 
-// O_i (+)= P_i V for one 128-key tile: 4 MMAs of K = 32; P_i (e4m3, written
-// by the softmax warps) and V^T both in shared memory, 128-byte swizzled.
+// O_i (+)= P_i V for one 128-key tile: 4 MMAs of M = 128, N = D, K = 32;
+// P_i (e4m3, written by the softmax warps) and V^T both in shared memory,
+// 128-byte swizzled.
+template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint64_t dp, uint64_t dv, bool acc) {
+  constexpr uint32_t idesc = D == 128 ? tc::kIdescM128N128 : tc::kIdescM128N64;
 #pragma unroll
   for (int ks = 0; ks < 4; ++ks)
-    tc::mma_f8_ss(d_tmem, desc_at(dp, 32u * ks), desc_at(dv, 32u * ks), tc::kIdescM128N128,
-                  (acc || ks > 0) ? 1u : 0u);
+    tc::mma_f8_ss(d_tmem, desc_at(dp, 32u * ks), desc_at(dv, 32u * ks), idesc, (acc || ks > 0) ? 1u : 0u);
 }
 
 // One lane of the warp, chosen by the hardware (elect.sync).
@@ -213,7 +224,7 @@ __device__ __forceinline__ bool elect_one() {
 // with P and O, writes e4m3(p448) into the shared-memory P tile and rescales O
 // when the maximum grew. kTail masks keys at or past nvalid (the last tile of a
 // ragged S). Returns false if a bounded wait ran out.
-template <bool kTail>
+template <int D, bool kTail>
 __device__ __forceinline__ bool softmax_tile(const Ctx& cx, int i, uint32_t tS, uint32_t tO, uint8_t* p_row, int row,
                                              const float (&cb)[4], int nvalid, bool first, uint32_t& pv_cnt,
                                              float& m, float& l) {
@@ -286,13 +297,13 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& cx, int i, uint32_t tS, 
         make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
   tc::fence_proxy_async_smem();
   if (!first && __any_sync(0xffffffffu, grew)) {
-    uint32_t o[4][32];
+    uint32_t o[D / 32][32];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tc::tmem_ld32(tO + 32u * c, o[c]);
+    for (int c = 0; c < D / 32; ++c) tc::tmem_ld32(tO + 32u * c, o[c]);
     tc::tmem_wait_ld();
     const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
         const float2 r = __fmul2_rn(make_float2(__uint_as_float(o[c][k]), __uint_as_float(o[c][k + 1])), a2);
@@ -306,19 +317,21 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& cx, int i, uint32_t tS, 
   return true;
 }
 
-// kCausal: the causal mask (a separate instantiation, so the unmasked kernel
-// carries none of its branches).
-template <bool kCausal>
+// D: the head dimension (128 or 64). kCausal: the causal mask (a separate
+// instantiation, so the unmasked kernel carries none of its branches).
+template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+  using L = Smem<D>;
+  using T = SmemTail<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = tc::smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctx cx;
-  cx.bar0 = sbase + kOffBar;
-  cx.abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  cx.bar0 = sbase + L::kOffBar;
+  cx.abort_flag = reinterpret_cast<volatile int*>(smem + T::kOffAbort);
   cx.dev_err = prm.dev_err;
 
   if (threadIdx.x == 0) {
@@ -344,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+    tc::tmem_alloc(sbase + T::kOffTmemSlot, kTmemCols);
     tc::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -355,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + T::kOffTmemSlot);
 
   if (warp < 4) {
     // control warpgroup: one register decrease for all four warps
@@ -373,12 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t q_row0 = static_cast<int32_t>((u % prm.pairs_per_head) * 256);
           // both query tiles (two 64-channel boxes each)
           if (!(ok = wait_bar(cx, cx.bar(kBarQEmpty), (u_cnt & 1u) ^ 1u))) break;
-          tc::mbar_arrive_expect_tx(cx.bar(kBarQFull), 2 * kTile16);
+          tc::mbar_arrive_expect_tx(cx.bar(kBarQFull), 2 * L::kTile16);
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int x = 0; x < 2; ++x)
-              tc::tma_load_3d(sbase + kOffQ16 + t * kTile16 + x * kSub16, &tm_q, 64 * x, q_row0 + 128 * t, bh,
+            for (int x = 0; x < D / 64; ++x)
+              tc::tma_load_3d(sbase + L::kOffQ16 + t * L::kTile16 + x * kSub16, &tm_q, 64 * x, q_row0 + 128 * t, bh,
                               cx.bar(kBarQFull));
           q_pending = static_cast<int>(u_cnt & 1u);
           ++u_cnt;
@@ -387,17 +400,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int64_t j = 0; ok && j < n_kv_u; ++j) {
             const uint32_t ks = k_cnt % kKStages, kph = (k_cnt / kKStages) & 1u;
             if (!(ok = wait_bar(cx, cx.bar(kBarKEmpty + ks), kph ^ 1u))) break;
-            tc::mbar_arrive_expect_tx(cx.bar(kBarKFull + ks), kTile16);
+            tc::mbar_arrive_expect_tx(cx.bar(kBarKFull + ks), L::kTile16);
 #pragma unroll
-            for (int x = 0; x < 2; ++x)
-              tc::tma_load_3d(sbase + kOffK16 + ks * kTile16 + x * kSub16, &tm_k, 64 * x,
+            for (int x = 0; x < D / 64; ++x)
+              tc::tma_load_3d(sbase + L::kOffK16 + ks * L::kTile16 + x * kSub16, &tm_k, 64 * x,
                               static_cast<int32_t>(j) * 128, bh, cx.bar(kBarKFull + ks));
             k_pending[ks] = static_cast<int>(kph);
             ++k_cnt;
             const uint32_t vs = v_cnt % kVStages, vph = (v_cnt / kVStages) & 1u;
             if (!(ok = wait_bar(cx, cx.bar(kBarVEmpty + vs), vph ^ 1u))) break;
-            tc::mbar_arrive_expect_tx(cx.bar(kBarVFull + vs), kTile8);
-            tc::tma_load_3d(sbase + kOffV + vs * kTile8, &tm_v, static_cast<int32_t>(j) * 128, 0, bh,
+            tc::mbar_arrive_expect_tx(cx.bar(kBarVFull + vs), L::kTileV);
+            tc::tma_load_3d(sbase + L::kOffV + vs * L::kTileV, &tm_v, static_cast<int32_t>(j) * 128, 0, bh,
                             cx.bar(kBarVFull + vs));
             v_pending[vs] = static_cast<int>(vph);
             ++v_cnt;
@@ -422,11 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // issues the MMAs and commits.
       const int i = warp - 1;
       const bool leader = elect_one();
-      const uint32_t d_s = tmem + col_s(i), d_o = tmem + col_o(i);
-      const uint64_t dq = tc::sw128_desc(sbase + kOffQ16 + static_cast<uint32_t>(i) * kTile16);
-      const uint64_t dk0 = tc::sw128_desc(sbase + kOffK16);
-      const uint64_t dv0 = tc::sw128_desc(sbase + kOffV);
-      const uint64_t dp = tc::sw128_desc(sbase + kOffP + static_cast<uint32_t>(i) * kTile8);
+      const uint32_t d_s = tmem + col_s(i), d_o = tmem + col_o<D>(i);
+      const uint64_t dq = tc::sw128_desc(sbase + L::kOffQ16 + static_cast<uint32_t>(i) * L::kTile16);
+      const uint64_t dk0 = tc::sw128_desc(sbase + L::kOffK16);
+      const uint64_t dv0 = tc::sw128_desc(sbase + L::kOffV);
+      const uint64_t dp = tc::sw128_desc(sbase + L::kOffP + static_cast<uint32_t>(i) * kTile8);
       uint32_t k_cnt = 0, v_cnt = 0, u_cnt = 0, sf_cnt = 0, p_cnt = 0;
       bool ok = true;
       for (int64_t u = blockIdx.x; ok && u < prm.n_units; u += gridDim.x) {
@@ -447,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               tc::tc_fence_after();
               if (leader) {
-                issue_qk(d_s, dq, desc_at(dk0, ks * kTile16));
+                issue_qk<D>(d_s, dq, desc_at(dk0, ks * L::kTile16));
                 tc::mma_commit(cx.bar(kBarSFull + i));
                 tc::mma_commit(cx.bar(kBarKEmpty + ks));
                 if (j == n_kv_i - 1) tc::mma_commit(cx.bar(kBarQEmpty));
@@ -469,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (jj == 0 && !(ok = wait_bar_warp(cx, cx.bar(kBarOEmpty + i), (u_cnt & 1u) ^ 1u))) break;
               tc::tc_fence_after();
               if (leader) {
-                issue_pv(d_o, dp, desc_at(dv0, vs * kTile8), jj > 0);
+                issue_pv<D>(d_o, dp, desc_at(dv0, vs * L::kTileV), jj > 0);
                 tc::mma_commit(cx.bar(kBarPVDone + i));
                 tc::mma_commit(cx.bar(kBarVEmpty + vs));
               }
@@ -499,8 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = wq * 32 + lane;       // row within the query tile
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_addr + col_s(i);
-    const uint32_t tO = tmem + lane_addr + col_o(i);
-    uint8_t* p_row = smem + kOffP + static_cast<uint32_t>(i) * kTile8 + row * 128;
+    const uint32_t tO = tmem + lane_addr + col_o<D>(i);
+    uint8_t* p_row = smem + L::kOffP + static_cast<uint32_t>(i) * kTile8 + row * 128;
     const int64_t nblk = prm.S_pad / kQKBlock;
     uint32_t s_cnt = 0, pv_cnt = 0;
     bool ok = true;
@@ -537,8 +550,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t lim = below_s < kKeyTile ? below_s : kKeyTile;
         if (diagonal && lim > row + 1) lim = row + 1;
         ok = !(diagonal || below_s < kKeyTile)
-                 ? softmax_tile<false>(cx, i, tS, tO, p_row, row, cb, kKeyTile, j == 0, pv_cnt, m, l)
-                 : softmax_tile<true>(cx, i, tS, tO, p_row, row, cb, static_cast<int>(lim), j == 0, pv_cnt, m, l);
+                 ? softmax_tile<D, false>(cx, i, tS, tO, p_row, row, cb, kKeyTile, j == 0, pv_cnt, m, l)
+                 : softmax_tile<D, true>(cx, i, tS, tO, p_row, row, cb, static_cast<int>(lim), j == 0, pv_cnt, m,
+                                         l);
         if (!ok) break;
         tc::tc_fence_before();
         tc::mbar_arrive(cx.bar(kBarPFull + i));
@@ -555,11 +569,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // logits in base 2, l counting 448 * 2^(x - m)
         prm.lse[bh * prm.S + qrow] = (m + log2f(l) - kLog2P) * kLn2;
       }
-      const float* sv = prm.v_scale + bh * kHeadDim;
+      const float* sv = prm.v_scale + bh * D;
       const int64_t b_idx = bh / prm.H, h_idx = bh % prm.H;
       uint16_t* dst = prm.out.p + b_idx * prm.out.sb + qrow * prm.out.ss + h_idx * prm.out.sh;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tc::tmem_ld32(tO + 32u * c, o);
         tc::tmem_wait_ld();
@@ -592,29 +606,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// 3-D tensor [d2][d1][d0] of `esize`-byte elements; boxes of box0 x 128 x 1
+// 3-D tensor [d2][d1][d0] of `esize`-byte elements; boxes of box0 x box1 x 1
 // elements with the 128-byte swizzle (box0 * esize must be 128).
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base, uint64_t d0, uint64_t d1,
-              uint64_t d2, uint32_t box0) {
+              uint64_t d2, uint32_t box0, uint32_t box1) {
   const uint64_t dims[3] = {d0, d1, d2};
   const uint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
-  const uint32_t box[3] = {box0, 128, 1};
+  const uint32_t box[3] = {box0, box1, 1};
   return make_tmap(m, dt, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
 
-cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale, const Out& out,
-                                bool causal, float* lse, int* dev_err, cudaStream_t stream) {
+cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
+                                const Out& out, bool causal, float* lse, int* dev_err, cudaStream_t stream) {
+  if (D != 128 && D != 64) return cudaErrorInvalidValue;
   const int64_t S_pad = padded_len(S);
   const int64_t BH = B * H;
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, in.q16, kHeadDim, static_cast<uint64_t>(S_pad),
-                static_cast<uint64_t>(BH), 64) ||
-      !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, in.k16, kHeadDim, static_cast<uint64_t>(S_pad),
-                static_cast<uint64_t>(BH), 64) ||
-      !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in.vt_codes, static_cast<uint64_t>(S_pad), kHeadDim,
-                static_cast<uint64_t>(BH), 128))
+  const uint64_t d = static_cast<uint64_t>(D);
+  if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, in.q16, d, static_cast<uint64_t>(S_pad),
+                static_cast<uint64_t>(BH), 64, 128) ||
+      !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, in.k16, d, static_cast<uint64_t>(S_pad),
+                static_cast<uint64_t>(BH), 64, 128) ||
+      !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in.vt_codes, static_cast<uint64_t>(S_pad), d,
+                static_cast<uint64_t>(BH), 128, static_cast<uint32_t>(D)))
     return cudaErrorInvalidValue;
   Params p;
   p.S = S;
@@ -630,13 +646,15 @@ cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t 
   p.sm_log2 = sm_scale * kLog2e;
   p.lse = lse;
   p.dev_err = dev_err;
-  auto kernel = causal ? attention_tc_kernel<true> : attention_tc_kernel<false>;
+  auto kernel = D == 128 ? (causal ? attention_tc_kernel<128, true> : attention_tc_kernel<128, false>)
+                         : (causal ? attention_tc_kernel<64, true> : attention_tc_kernel<64, false>);
+  const uint32_t smem_bytes = D == 128 ? SmemTail<128>::kBytes : SmemTail<64>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+                                       static_cast<int>(smem_bytes));
   if (e != cudaSuccess) return e;
   const int sms = sm_count_current();
   const int grid = static_cast<int>(p.n_units < sms ? p.n_units : sms);
-  kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  kernel<<<grid, kThreads, smem_bytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -8,7 +8,7 @@
 
 namespace sage {
 
-constexpr int kHeadDim = 128;     // the only supported head dimension
+constexpr int kHeadDim = 128;     // the head dimension of the pages' workload (64 is also supported)
 constexpr int kQKBlock = 32;      // tokens per Q/K scale block ("per 32-row block")
 constexpr int kKeyTile = 128;     // keys per online-softmax step; S is padded to this
 constexpr float kInt8Max = 127.0f;
@@ -57,13 +57,18 @@ size_t l2_bytes_current();     // L2 bytes of the current device (cached)
 // `stream` and returns the launch status (cudaGetLastError).
 // write_int8: also store the int8 Q/K codes (the fp16 copies, V codes and
 // all scales are always written). dev_err: the device error word.
+// D: the head dimension (128 or 64).
 cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, int64_t B, int64_t S,
-                            int64_t H, bool smooth_k, const Bundle& out, void* scratch, bool write_int8,
+                            int64_t H, int64_t D, bool smooth_k, const Bundle& out, void* scratch, bool write_int8,
                             int* dev_err, cudaStream_t stream);
+// The head-dimension-64 prologue (three plain kernels) and its scratch.
+cudaError_t launch_prologue64(const Bf16In& q, const Bf16In& k, const Bf16In& v, int64_t B, int64_t S, int64_t H,
+                              bool smooth_k, const Bundle& out, void* scratch, bool write_int8, cudaStream_t stream);
+size_t prologue64_scratch_bytes(int64_t B, int64_t S, int64_t H);
 // Device address of the current device's error word (set up on first use),
 // or nullptr if the runtime call fails.
 int* device_error_ptr();
-size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H);
+size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H, int64_t D);
 
 cudaError_t launch_attention_simt(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale,
                                   const Out& out, bool causal, float* lse, cudaStream_t stream);
@@ -71,12 +76,12 @@ cudaError_t launch_attention_simt(const Bundle& in, int64_t B, int64_t S, int64_
 // causal: query i sees keys j <= i only. lse: null, or [B][H][S] fp32 that
 // receives each row's natural-log log-sum-exp of its logits (of the keys the
 // bundle holds, i.e. of k - mean when it was quantized with smooth_k).
-cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale,
+cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
                                 const Out& out, bool causal, float* lse, int* dev_err, cudaStream_t stream);
 
 // Adds sm_scale * q_i . k_mean to lse[b][h][i] (the smooth_k term that turns
 // the log-sum-exp of the mean-reduced keys into that of the original keys).
 cudaError_t launch_lse_smooth_k_term(const Bf16In& q, const float* k_mean, int64_t B, int64_t S, int64_t H,
-                                     float sm_scale, float* lse, cudaStream_t stream);
+                                     int64_t D, float sm_scale, float* lse, cudaStream_t stream);
 
 }  // namespace sage

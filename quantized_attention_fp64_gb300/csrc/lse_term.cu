@@ -11,8 +11,8 @@
 // "What changed" (the smooth_k key mean).
 //
 // Bandwidth-bound: it reads Q once (2 bytes per element). One warp per row,
-// 4 channels per lane (8-byte loads, one 256-byte row per warp instruction),
-// 8 rows per warp, the row loads issued before the reductions.
+// D / 32 channels per lane (one whole row per warp instruction), 8 rows per
+// warp, the row loads issued before the reductions.
 #include "common.cuh"
 
 namespace sage {
@@ -21,24 +21,32 @@ namespace {
 constexpr int kRowsPerWarp = 8;
 constexpr int kWarpsPerBlock = 8;
 
+template <int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     lse_term_kernel(Bf16In q, const float* __restrict__ k_mean, int64_t S, int64_t H, float sm_scale,
                     float* __restrict__ lse) {
+  constexpr int kW = D / 64;  // bf16x2 words per lane
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t b = blockIdx.z, h = blockIdx.y, bh = b * H + h;
   const int64_t s0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp) * kRowsPerWarp;
-  const float4 mu = __ldg(reinterpret_cast<const float4*>(k_mean + bh * kHeadDim + 4 * lane));
-  const uint16_t* base = q.p + b * q.sb + h * q.sh + 4 * lane;
-  uint2 w[kRowsPerWarp];
+  float mu[2 * kW];
+#pragma unroll
+  for (int c = 0; c < 2 * kW; ++c) mu[c] = __ldg(k_mean + bh * D + 2 * kW * lane + c);
+  const uint16_t* base = q.p + b * q.sb + h * q.sh + 2 * kW * lane;
+  uint32_t w[kRowsPerWarp][kW];
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r)
-    w[r] = s0 + r < S ? __ldcs(reinterpret_cast<const uint2*>(base + (s0 + r) * q.ss)) : make_uint2(0u, 0u);
+#pragma unroll
+    for (int x = 0; x < kW; ++x)
+      w[r][x] = s0 + r < S ? __ldcs(reinterpret_cast<const unsigned int*>(base + (s0 + r) * q.ss) + x) : 0u;
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r) {
-    float d = __uint_as_float(w[r].x << 16) * mu.x;
-    d = fmaf(__uint_as_float(w[r].x & 0xFFFF0000u), mu.y, d);
-    d = fmaf(__uint_as_float(w[r].y << 16), mu.z, d);
-    d = fmaf(__uint_as_float(w[r].y & 0xFFFF0000u), mu.w, d);
+    float d = 0.0f;
+#pragma unroll
+    for (int x = 0; x < kW; ++x) {
+      d = fmaf(__uint_as_float(w[r][x] << 16), mu[2 * x], d);
+      d = fmaf(__uint_as_float(w[r][x] & 0xFFFF0000u), mu[2 * x + 1], d);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
     if (lane == 0 && s0 + r < S) lse[bh * S + s0 + r] += sm_scale * d;
@@ -48,11 +56,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 }  // namespace
 
 cudaError_t launch_lse_smooth_k_term(const Bf16In& q, const float* k_mean, int64_t B, int64_t S, int64_t H,
-                                     float sm_scale, float* lse, cudaStream_t stream) {
+                                     int64_t D, float sm_scale, float* lse, cudaStream_t stream) {
   const int64_t rows_per_block = static_cast<int64_t>(kRowsPerWarp) * kWarpsPerBlock;
   const dim3 grid(static_cast<unsigned>(div_up(S, rows_per_block)), static_cast<unsigned>(H),
                   static_cast<unsigned>(B));
-  lse_term_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(q, k_mean, S, H, sm_scale, lse);
+  if (D == 128)
+    lse_term_kernel<128><<<grid, kWarpsPerBlock * 32, 0, stream>>>(q, k_mean, S, H, sm_scale, lse);
+  else if (D == 64)
+    lse_term_kernel<64><<<grid, kWarpsPerBlock * 32, 0, stream>>>(q, k_mean, S, H, sm_scale, lse);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

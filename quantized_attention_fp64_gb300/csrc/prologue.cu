@@ -1110,11 +1110,14 @@ int make_input_map(CUtensorMap* m, const Bf16In& t, int64_t B, int64_t S, int64_
 
 }  // namespace
 
-size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H) { return scratch_layout(B, S, H).total; }
+size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H, int64_t D) {
+  return D == kHeadDim ? scratch_layout(B, S, H).total : prologue64_scratch_bytes(B, S, H);
+}
 
 cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, int64_t B, int64_t S, int64_t H,
-                            bool smooth_k, const Bundle& out, void* scratch, bool write_int8, int* dev_err,
-                            cudaStream_t stream) {
+                            int64_t D, bool smooth_k, const Bundle& out, void* scratch, bool write_int8,
+                            int* dev_err, cudaStream_t stream) {
+  if (D != kHeadDim) return launch_prologue64(q, k, v, B, S, H, smooth_k, out, scratch, write_int8, stream);
   const ScratchLayout l = scratch_layout(B, S, H);
   char* sc = static_cast<char*>(scratch);
   Params p;

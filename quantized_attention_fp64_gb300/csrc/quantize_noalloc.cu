@@ -91,7 +91,7 @@ extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_
                                      const sage_bf16_tensor* v, int64_t B, int64_t S, int64_t H, int64_t D,
                                      int smooth_k, const sage_quantized* out, void* cuda_stream) {
   if (B < 0 || S < 0 || H < 0 || D < 0) return SAGE_ERR_SHAPE;
-  if (D != kHeadDim) return SAGE_ERR_HEAD_DIM;
+  if (D != kHeadDim && D != 64) return SAGE_ERR_HEAD_DIM;
   if (B > 65535 || H > 65535 || S > (int64_t(1) << 31)) return SAGE_ERR_TOO_LARGE;
   int rc;
   if ((rc = check_in(q)) != SAGE_OK || (rc = check_in(k)) != SAGE_OK || (rc = check_in(v)) != SAGE_OK) return rc;
@@ -104,7 +104,7 @@ extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_
   }
   // the built-in buffer bounds the problem size: B * H * ceil(S / 128) groups
   // of 128 channels, 12 bytes each (plus alignment)
-  if (prologue_scratch_bytes(B, S, H) > kNoAllocScratch) return SAGE_ERR_WORKSPACE;
+  if (prologue_scratch_bytes(B, S, H, D) > kNoAllocScratch) return SAGE_ERR_WORKSPACE;
   void* scratch = noalloc_scratch_ptr(&rc);
   if (scratch == nullptr) return rc;
   if (B == 0 || H == 0 || S == 0) return SAGE_OK;
@@ -115,7 +115,7 @@ extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_
                   out->v_scale_dev, out->k_mean_dev,  out->q16_dev,      out->k16_dev};
   int* dev_err = device_error_ptr();
   if (dev_err == nullptr) return SAGE_ERR_CUDA;
-  const cudaError_t e = launch_prologue(qi, ki, vi, B, S, H, smooth_k != 0, bo, scratch, true, dev_err,
+  const cudaError_t e = launch_prologue(qi, ki, vi, B, S, H, D, smooth_k != 0, bo, scratch, true, dev_err,
                                         static_cast<cudaStream_t>(cuda_stream));
   return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA;
 }

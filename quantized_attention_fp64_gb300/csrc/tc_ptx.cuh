@@ -180,6 +180,8 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // Instruction descriptor: fp32 accumulator, both operands K-major, A/B type
 // code 0 (f16 for kind::f16, e4m3 for kind::f8f6f4), N = 128, M = 128.
 constexpr uint32_t kIdescM128N128 = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+// The same with N = 64.
+constexpr uint32_t kIdescM128N64 = (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
 
 // D(tmem) (+)= A(smem) * B(smem)^T, f16 x f16 -> f32, K = 16.
 __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

@@ -4,7 +4,8 @@ This module holds no arithmetic of the method; it only draws the BF16 Q, K
 and V tensors that both the library and the test oracle consume. Shapes and
 value distributions follow the five benchmark configurations (diffusion
 self-attention with 28 heads of dimension 128 at image and video sizes, plus
-a long-sequence case past 100k tokens). Each tensor is drawn in fp32 from a
+a long-sequence case past 100k tokens), and head dimension 64 (the pages'
+second workload) at the image and video sizes. Each tensor is drawn in fp32 from a
 torch generator seeded with ``1000 + index`` (per-channel key offsets use the
 next seed) and rounded to bf16.
 """
@@ -30,11 +31,12 @@ class Workload:
     outlier_p: float = 0.0      # probability that a Q or K entry is scaled by outlier_scale
     outlier_scale: float = 8.0
     smooth_k: bool = True
+    D: int = 128                # head dimension
 
     @property
     def attention_ops(self) -> int:
         """4 * B * H * S^2 * D: the multiply-adds of QK^T and PV, counted as 2 ops each."""
-        return 4 * self.B * self.H * self.S * self.S * 128
+        return 4 * self.B * self.H * self.S * self.S * self.D
 
 
 WORKLOADS = {
@@ -46,6 +48,8 @@ WORKLOADS = {
         Workload("B1_H28_S16384", 3, 1, 28, 16384, q_std=1.5, k_std=1.5, outlier_p=0.01),
         Workload("B1_H28_S131072", 4, 1, 28, 131072, k_offset_std=2.0),
         Workload("B1_H80_S131072", 5, 1, 80, 131072, k_offset_std=2.0),
+        Workload("B1_H28_S4096_D64", 6, 1, 28, 4096, k_offset_std=2.0, D=64),
+        Workload("B1_H28_S16384_D64", 7, 1, 28, 16384, q_std=1.5, k_std=1.5, outlier_p=0.01, D=64),
     ]
 }
 
@@ -55,12 +59,12 @@ def custom(B: int, H: int, S: int, seed_index: int = 100, **kw) -> Workload:
 
 
 def make_qkv(w: Workload, device="cuda", layout: str = "NHD"):
-    """Draws (q, k, v) as BF16 tensors of shape [B,S,H,128] ("NHD") or
-    [B,H,S,128] ("HND"), contiguous, on ``device``."""
+    """Draws (q, k, v) as BF16 tensors of shape [B,S,H,D] ("NHD") or
+    [B,H,S,D] ("HND"), contiguous, on ``device``."""
     device = torch.device(device)
     gen = torch.Generator(device=device)
     gen.manual_seed(1000 + w.index)
-    shape = (w.B, w.S, w.H, 128)
+    shape = (w.B, w.S, w.H, w.D)
 
     def draw(std, outliers):
         x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
@@ -81,7 +85,7 @@ def make_qkv(w: Workload, device="cuda", layout: str = "NHD"):
     if w.k_offset_std > 0:
         g2 = torch.Generator(device=device)
         g2.manual_seed(1000 + w.index + 1)
-        off = torch.randn((w.H, 128), generator=g2, device=device, dtype=torch.float32) * w.k_offset_std
+        off = torch.randn((w.H, w.D), generator=g2, device=device, dtype=torch.float32) * w.k_offset_std
         k32.add_(off[None, None])
     k = k32.to(torch.bfloat16)
     del k32

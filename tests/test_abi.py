@@ -56,7 +56,8 @@ def test_size_queries(lib):
     # scratch: a 256-byte work counter, two per-head flag arrays (256-aligned),
     # then fp64 + fp32 per (head, 128-token group, channel)
     assert sc == 256 + 2 * 256 + 28 * 128 * 128 * 8 + 28 * 128 * 128 * 4
-    assert _sizes(lib, "sage_workspace_size", 1, 100, 2, 64)[0] == HEAD_DIM
+    assert _sizes(lib, "sage_workspace_size", 1, 100, 2, 96)[0] == HEAD_DIM
+    assert _sizes(lib, "sage_workspace_size", 1, 100, 2, 64)[0] == OK
     assert _sizes(lib, "sage_workspace_size", -1, 100, 2, 128)[0] == SHAPE
     assert _sizes(lib, "sage_workspace_size", 1, 2 ** 40, 2, 128)[0] == TOO_LARGE
     assert _sizes(lib, "sage_workspace_size", 0, 0, 0, 128)[0] == OK
@@ -118,7 +119,7 @@ def test_quantize_and_attention_rejections(lib):
     qz = _lib.Quantized(0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000, 0x800000,
                         0x900000)
     r = ctypes.byref
-    assert lib.sage_quantize(r(t), r(t), r(t), 1, 256, 2, 64, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == HEAD_DIM
+    assert lib.sage_quantize(r(t), r(t), r(t), 1, 256, 2, 96, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == HEAD_DIM
     assert lib.sage_quantize(r(bad), r(t), r(t), 1, 256, 2, 128, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == ALIGN
     assert lib.sage_quantize(r(t), r(nul), r(t), 1, 256, 2, 128, 1, r(qz), ctypes.c_void_p(0x800000), 1 << 30, None) == NULLPTR
     assert lib.sage_quantize(r(t), r(t), r(t), 1, 256, 2, 128, 1, r(qz), ctypes.c_void_p(0x800000), 16, None) == WORKSPACE
@@ -145,7 +146,7 @@ def test_quantize_and_attention_rejections(lib):
                                       ctypes.c_void_p(0xA00002), None) == ALIGN
     assert lib.sage_lse_smooth_k_term(r(t), None, 1, 256, 2, 128, ctypes.c_float(0.1),
                                       ctypes.c_void_p(0xA00000), None) == NULLPTR
-    assert lib.sage_lse_smooth_k_term(r(t), ctypes.c_void_p(0x700000), 1, 256, 2, 64, ctypes.c_float(0.1),
+    assert lib.sage_lse_smooth_k_term(r(t), ctypes.c_void_p(0x700000), 1, 256, 2, 96, ctypes.c_float(0.1),
                                       ctypes.c_void_p(0xA00000), None) == HEAD_DIM
 
 
@@ -172,7 +173,7 @@ def _call_sageattn_ex(lib, lse_ptr=0x60000, **over):
 
 @pytest.mark.parametrize("over,code", [
     (dict(dt=1), DTYPE), (dict(odt=1), DTYPE),
-    (dict(shape=(1, 256, 2, 64)), HEAD_DIM),
+    (dict(shape=(1, 256, 2, 96)), HEAD_DIM),
     (dict(kshape=(1, 255, 2, 128)), SHAPE),
     (dict(layout=b"BSHD"), LAYOUT),
     (dict(out=0x40004), ALIGN), (dict(lse_ptr=0x60002), ALIGN),
