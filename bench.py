@@ -323,6 +323,16 @@ def run_gpu(args):
     # query tile cannot see, so it does the visible half of the work
     t_att_causal = graph_time(lambda: attention(qz, sm, out=out, is_causal=True))
     ops_causal = 4.0 * B * H * D * (S * (S + 1) / 2)
+    # head dimension 64 at the same size (the pages' second workload): the
+    # plain three-kernel prologue and the D = 64 attention kernel
+    w64 = WORKLOADS["B1_H28_S16384_D64"]
+    q64, k64, v64 = make_qkv(w64, "cuda")
+    qz64 = alloc_bundle(w64.B, w64.S, w64.H, q64.device, 64)
+    out64 = torch.empty_like(q64)
+    sm64 = 1.0 / math.sqrt(64.0)
+    t_pro64 = graph_time(lambda: quantize(q64, k64, v64, "NHD", True, out=qz64))
+    t_att64 = graph_time(lambda: attention(qz64, sm64, out=out64))
+    del q64, k64, v64, qz64, out64
     if device_error() != 0:
         raise RuntimeError("device error word set during timing")
 
@@ -388,6 +398,12 @@ def run_gpu(args):
                      "gbs": pro_bytes / t_pro / 1e9, "frac_of_hbm": pro_bytes / t_pro / 1e9 / peaks["hbm_gbs"],
                      "bytes_written_and_read": pro_moved, "gbs_moved": pro_moved / t_pro / 1e9,
                      "peak_gbs": peaks["hbm_gbs"], "bound": "hbm"},
+        "head_dim_64": {"workload": "B1_H28_S16384_D64", "attention_ms": t_att64 * 1e3,
+                        "attention_tflops": float(w64.attention_ops) / t_att64 / 1e12,
+                        "attention_frac_of_peak": float(w64.attention_ops) / t_att64 / 1e12 / p_att,
+                        "prologue_ms": t_pro64 * 1e3,
+                        "prologue_gbs": 9 * w64.B * w64.H * w64.S * 64 / t_pro64 / 1e9,
+                        "prologue_frac_of_hbm": 9 * w64.B * w64.H * w64.S * 64 / t_pro64 / 1e9 / peaks["hbm_gbs"]},
         "e2e": {"value": world * ops / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": 3 * 2 * n_elem,
                 "d2h_bytes_per_step": 2 * n_elem, "ms_per_step": t_e2e * 1e3},
         # per step: the prologue kernel and the attention kernel (plus one
