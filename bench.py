@@ -247,6 +247,65 @@ def run_profile(args):
     return 0
 
 
+def short_call_latency(torch, sageattn, sm):
+    """Short calls (a few hundred tokens, where the host work and the kernel
+    launches dominate): the latency of one sageattn call at a time, from
+    CUDA events around the call (host marshalling, the cluster prologue and
+    the attention kernel) and from the wall clock including a synchronize,
+    beside torch's bf16 scaled_dot_product_attention timed the same way.
+    Also the first call of a fresh process (library load included)."""
+    import statistics
+
+    from quantized_attention_fp64_gb300.workloads import custom, make_qkv
+
+    def one_at_a_time(fn, reps=50, warm=10):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        ev, wall = [], []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            wall.append((time.perf_counter() - t0) * 1e6)
+            ev.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ev), statistics.median(wall)
+
+    rows = []
+    for (b_, h_, s_) in ((1, 28, 256), (1, 28, 512), (1, 28, 1024), (2, 8, 1024)):
+        qs, ks, vs = make_qkv(custom(b_, h_, s_, seed_index=5000 + s_, k_offset_std=2.0), "cuda")
+        qt, kt, vt = (x.transpose(1, 2) for x in (qs, ks, vs))
+        ours_ev, ours_wall = one_at_a_time(lambda: sageattn(qs, ks, vs, sm_scale=sm))
+        ref_ev, ref_wall = one_at_a_time(
+            lambda: torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=sm))
+        rows.append({"workload": f"B{b_}_H{h_}_S{s_}", "sageattn_us": round(ours_ev, 2),
+                     "sageattn_wall_us": round(ours_wall, 2), "sdpa_bf16_us": round(ref_ev, 2),
+                     "sdpa_bf16_wall_us": round(ref_wall, 2), "ratio": round(ours_ev / ref_ev, 3)})
+    code = ("import time, torch\n"
+            "from quantized_attention_fp64_gb300.workloads import custom, make_qkv\n"
+            "q, k, v = make_qkv(custom(1, 28, 256, seed_index=5256), 'cuda')\n"
+            "torch.cuda.synchronize()\n"
+            "t0 = time.perf_counter()\n"
+            "from quantized_attention_fp64_gb300 import sageattn\n"
+            "sageattn(q, k, v)\n"
+            "torch.cuda.synchronize()\n"
+            "print(time.perf_counter() - t0)\n")
+    first = None
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+        if r.returncode == 0:
+            first = float(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError):
+        first = None
+    return {"timing": "one call at a time: median of 50 (CUDA events around the call; wall clock with a "
+                      "synchronize)", "reference": "torch.nn.functional.scaled_dot_product_attention, bf16",
+            "rows": rows, "first_call_s": first,
+            "first_call_note": "fresh process, B1 H28 S256: library load, module load and the call"}
+
+
 def run_gpu(args):
     import torch
 
@@ -335,6 +394,7 @@ def run_gpu(args):
     del q64, k64, v64, qz64, out64
     if device_error() != 0:
         raise RuntimeError("device error word set during timing")
+    short_calls = short_call_latency(torch, sageattn, sm) if rank == 0 else None
 
     # --- end to end through the C ABI with pinned host buffers
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
@@ -404,6 +464,7 @@ def run_gpu(args):
                         "prologue_ms": t_pro64 * 1e3,
                         "prologue_gbs": 9 * w64.B * w64.H * w64.S * 64 / t_pro64 / 1e9,
                         "prologue_frac_of_hbm": 9 * w64.B * w64.H * w64.S * 64 / t_pro64 / 1e9 / peaks["hbm_gbs"]},
+        "short_calls": short_calls,
         "e2e": {"value": world * ops / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": 3 * 2 * n_elem,
                 "d2h_bytes_per_step": 2 * n_elem, "ms_per_step": t_e2e * 1e3},
         # per step: the prologue kernel and the attention kernel (plus one

@@ -153,9 +153,14 @@ SAGE_API int sage_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, siz
  * q, k, v: BF16 tensors of shape (B, S, H, 128) with the given strides.
  * scratch_dev: at least sage_quantize_scratch_size bytes, 256-byte aligned;
  * its contents on entry do not matter and are clobbered.
- * Enqueued: a clear of the scratch header (work counter, per-head flags) and
- * one persistent kernel that computes the statistics and Q codes, finishes
- * each head (key mean, V scales), then writes the K and V codes.
+ * Enqueued (D = 128): for S > 1024, a clear of the scratch header (work
+ * counter, per-head flags) and one persistent kernel that computes the
+ * statistics and Q codes, finishes each head (key mean, V scales), then
+ * writes the K and V codes; for S <= 1024, one kernel launched in clusters of
+ * ceil(S / 128) CTAs per head that exchange the head statistics through
+ * distributed shared memory and does not touch the scratch (which must still
+ * be passed, with the same size). Both give identical results.
+ * (D = 64: three plain kernels, statistics, head finish and codes.)
  * Errors: NULLPTR, SHAPE, HEAD_DIM, ALIGN, WORKSPACE, TOO_LARGE, ARCH, CUDA. */
 SAGE_API int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k, const sage_bf16_tensor* v,
                   int64_t B, int64_t S, int64_t H, int64_t D, int smooth_k,
@@ -194,6 +199,10 @@ SAGE_API int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_te
  * with fp32 accumulation in tensor memory, V scales in the epilogue.
  * out: BF16 (B, S, H, 128) at out_dev with element strides (ob, os, oh),
  * channel stride 1. sm_scale must be finite and > 0.
+ * The kernel is launched as a programmatic dependent of the previous kernel
+ * on the stream: it may start while that kernel (normally the prologue)
+ * still runs, and waits for it to complete before reading or writing
+ * global memory, so stream order holds as for a plain launch.
  * Errors: NULLPTR, SHAPE, HEAD_DIM, ALIGN, ARG, TOO_LARGE, ARCH, CUDA. */
 SAGE_API int sage_attention(const sage_quantized* in, int64_t B, int64_t S, int64_t H, int64_t D,
                    float sm_scale, void* out_dev, int64_t ob, int64_t os, int64_t oh,

@@ -15,6 +15,7 @@ from .api import (  # noqa: F401
     lse_smooth_k_term,
     quantize,
     quantize_scratch_size,
+    release_workspace_cache,
     sageattn,
     sageattn_ex,
     workspace_size,

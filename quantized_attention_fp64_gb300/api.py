@@ -219,6 +219,119 @@ def lse_smooth_k_term(q: torch.Tensor, qz: QuantizedQKV, lse: torch.Tensor, sm_s
     return lse
 
 
+# Per-call host work matters for short calls, so the sageattn entries keep it
+# small: shape and stride arrays are reused, the workspace of calls up to
+# _WS_CACHE_MAX bytes is kept per (device, stream) and reused by the next call
+# on that stream (stream order makes that safe), and the stream is read as a
+# raw handle.
+_WS_CACHE_MAX = 256 << 20
+_ws_cache: dict = {}
+_i64_cache: dict = {}
+_ws_size_cache: dict = {}
+_LAYOUTS = {"NHD": b"NHD", "HND": b"HND"}
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(index: int) -> int:
+    if _raw_stream is not None:
+        return _raw_stream(index)
+    return torch.cuda.current_stream(index).cuda_stream
+
+
+def _i64x4(t) -> "_lib.I64x4":
+    arr = _i64_cache.get(t)
+    if arr is None:
+        if len(_i64_cache) > 512:
+            _i64_cache.clear()
+        arr = _i64_cache[t] = _lib.I64x4(*t)
+    return arr
+
+
+def _ws_bytes(lib, B, S, H, D):
+    key = (B, S, H, D)
+    n = _ws_size_cache.get(key)
+    if n is None:
+        c = ctypes.c_size_t(0)
+        n = c.value if lib.sage_workspace_size(B, S, H, D, ctypes.byref(c)) == 0 else -1
+        if len(_ws_size_cache) > 512:
+            _ws_size_cache.clear()
+        _ws_size_cache[key] = n
+    return n
+
+
+def _workspace(device, stream: int, nbytes: int) -> torch.Tensor:
+    if nbytes > _WS_CACHE_MAX:
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    key = (device.index, stream)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def release_workspace_cache() -> None:
+    """Drops the workspaces kept for short sageattn calls."""
+    _ws_cache.clear()
+
+
+def _sageattn_call(ex: bool, q, k, v, tensor_layout, is_causal, sm_scale, return_lse, smooth_k, out, workspace):
+    for t in (q, k, v):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("expected torch tensors")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("tensors must live on a CUDA device")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise SageError(SAGE_ERR_SHAPE, "q, k and v must be 4-d")
+    lib = _lib.load()
+    layout = tensor_layout if isinstance(tensor_layout, str) else str(tensor_layout)
+    shape = tuple(q.shape)
+    B, S, H, D = _bsh(shape, layout)
+    ws_n = _ws_bytes(lib, B, S, H, D)
+    proceed = (ws_n >= 0 and layout in _LAYOUTS and q.dtype == k.dtype == v.dtype == torch.bfloat16
+               and shape == tuple(k.shape) == tuple(v.shape) and (ex or not (is_causal or return_lse)))
+    device = q.device
+    index = device.index
+    switch = index != torch.cuda.current_device()
+    ctx = torch.cuda.device(device) if switch else None
+    if ctx is not None:
+        ctx.__enter__()
+    try:
+        stream = _stream_handle(index)
+        lse = None
+        if proceed:
+            if out is None:
+                out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+            if workspace is None or workspace.numel() < ws_n:
+                workspace = _workspace(device, stream, ws_n)
+            if ex and return_lse:
+                lse = torch.empty((B, H, S), dtype=torch.float32, device=device)
+        out_ptr = out.data_ptr() if out is not None else None
+        out_strides = _i64x4(out.stride()) if out is not None else _i64x4((0, 0, 0, 1))
+        out_dtype = _dtype_code(out) if out is not None else 0
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_size = workspace.numel() if workspace is not None else 0
+        scale = float("nan") if sm_scale is None else float(sm_scale)
+        qs, ks, vs = _i64x4(shape), _i64x4(tuple(k.shape)), _i64x4(tuple(v.shape))
+        qst, kst, vst = _i64x4(q.stride()), _i64x4(k.stride()), _i64x4(v.stride())
+        lay = _LAYOUTS.get(layout) or layout.encode()
+        dq, dk, dv = _dtype_code(q), _dtype_code(k), _dtype_code(v)
+        if ex:
+            rc = lib.sage_sageattn_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), qs, ks, vs, qst, kst, vst, dq, dk, dv,
+                                      lay, int(bool(is_causal)), scale, int(bool(smooth_k)), out_ptr, out_strides,
+                                      out_dtype, lse.data_ptr() if lse is not None else None, ws_ptr, ws_size,
+                                      stream)
+        else:
+            rc = lib.sage_sageattn(q.data_ptr(), k.data_ptr(), v.data_ptr(), qs, ks, vs, qst, kst, vst, dq, dk, dv,
+                                   lay, int(bool(is_causal)), scale, int(bool(return_lse)), int(bool(smooth_k)),
+                                   out_ptr, out_strides, out_dtype, ws_ptr, ws_size, stream)
+    finally:
+        if ctx is not None:
+            ctx.__exit__(None, None, None)
+    _check(rc)
+    return (out, lse) if (ex and return_lse) else out
+
+
 def sageattn(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm_scale=None,
              return_lse: bool = False, smooth_k: bool = True, out=None, workspace=None) -> torch.Tensor:
     """sageattn(q, k, v, tensor_layout, is_causal, sm_scale, return_lse) through sage_sageattn.
@@ -226,38 +339,7 @@ def sageattn(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm_sc
     Unsupported inputs (causal, LSE, non-BF16, head dim != 128, unequal
     shapes, unknown layout) raise SageError; nothing falls back.
     """
-    _require_cuda(q, k, v)
-    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
-        raise SageError(SAGE_ERR_SHAPE, "q, k and v must be 4-d")
-    lib = _lib.load()
-    layout = tensor_layout if isinstance(tensor_layout, str) else str(tensor_layout)
-    B, S, H, D = _bsh(q.shape, layout)
-    ws_bytes = ctypes.c_size_t(0)
-    sizes_ok = lib.sage_workspace_size(B, S, H, D, ctypes.byref(ws_bytes)) == 0
-    proceed = (sizes_ok and not is_causal and not return_lse and layout in ("NHD", "HND")
-               and q.dtype == k.dtype == v.dtype == torch.bfloat16
-               and tuple(q.shape) == tuple(k.shape) == tuple(v.shape))
-    with torch.cuda.device(q.device):
-        if proceed and out is None:
-            out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-        if proceed and (workspace is None or workspace.numel() < ws_bytes.value):
-            workspace = torch.empty(max(ws_bytes.value, 256), dtype=torch.uint8, device=q.device)
-        out_ptr = out.data_ptr() if out is not None else None
-        out_strides = out.stride() if out is not None else (0, 0, 0, 1)
-        out_dtype = _dtype_code(out) if out is not None else 0
-        ws_ptr = workspace.data_ptr() if workspace is not None else None
-        ws_n = workspace.numel() if workspace is not None else 0
-        scale = float("nan") if sm_scale is None else float(sm_scale)
-        rc = lib.sage_sageattn(
-            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
-            _lib.I64x4(*q.shape), _lib.I64x4(*k.shape), _lib.I64x4(*v.shape),
-            _lib.I64x4(*q.stride()), _lib.I64x4(*k.stride()), _lib.I64x4(*v.stride()),
-            _dtype_code(q), _dtype_code(k), _dtype_code(v), layout.encode(), int(bool(is_causal)),
-            ctypes.c_float(scale), int(bool(return_lse)), int(bool(smooth_k)),
-            ctypes.c_void_p(out_ptr), _lib.I64x4(*out_strides), out_dtype,
-            ctypes.c_void_p(ws_ptr), ws_n, _stream(q.device))
-    _check(rc)
-    return out
+    return _sageattn_call(False, q, k, v, tensor_layout, is_causal, sm_scale, return_lse, smooth_k, out, workspace)
 
 
 def sageattn_ex(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm_scale=None,
@@ -266,40 +348,7 @@ def sageattn_ex(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm
     returns out, or (out, lse) with lse fp32 [B, H, S], the natural-log
     log-sum-exp of each query row's scaled logits. Other unsupported inputs
     raise SageError as in sageattn."""
-    _require_cuda(q, k, v)
-    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
-        raise SageError(SAGE_ERR_SHAPE, "q, k and v must be 4-d")
-    lib = _lib.load()
-    layout = tensor_layout if isinstance(tensor_layout, str) else str(tensor_layout)
-    B, S, H, D = _bsh(q.shape, layout)
-    ws_bytes = ctypes.c_size_t(0)
-    sizes_ok = lib.sage_workspace_size(B, S, H, D, ctypes.byref(ws_bytes)) == 0
-    proceed = (sizes_ok and layout in ("NHD", "HND") and q.dtype == k.dtype == v.dtype == torch.bfloat16
-               and tuple(q.shape) == tuple(k.shape) == tuple(v.shape))
-    lse = None
-    with torch.cuda.device(q.device):
-        if proceed and out is None:
-            out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-        if proceed and (workspace is None or workspace.numel() < ws_bytes.value):
-            workspace = torch.empty(max(ws_bytes.value, 256), dtype=torch.uint8, device=q.device)
-        if proceed and return_lse:
-            lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-        out_ptr = out.data_ptr() if out is not None else None
-        out_strides = out.stride() if out is not None else (0, 0, 0, 1)
-        out_dtype = _dtype_code(out) if out is not None else 0
-        ws_ptr = workspace.data_ptr() if workspace is not None else None
-        ws_n = workspace.numel() if workspace is not None else 0
-        scale = float("nan") if sm_scale is None else float(sm_scale)
-        rc = lib.sage_sageattn_ex(
-            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
-            _lib.I64x4(*q.shape), _lib.I64x4(*k.shape), _lib.I64x4(*v.shape),
-            _lib.I64x4(*q.stride()), _lib.I64x4(*k.stride()), _lib.I64x4(*v.stride()),
-            _dtype_code(q), _dtype_code(k), _dtype_code(v), layout.encode(), int(bool(is_causal)),
-            ctypes.c_float(scale), int(bool(smooth_k)), ctypes.c_void_p(out_ptr), _lib.I64x4(*out_strides),
-            out_dtype, ctypes.c_void_p(lse.data_ptr() if lse is not None else None),
-            ctypes.c_void_p(ws_ptr), ws_n, _stream(q.device))
-    _check(rc)
-    return (out, lse) if return_lse else out
+    return _sageattn_call(True, q, k, v, tensor_layout, is_causal, sm_scale, return_lse, smooth_k, out, workspace)
 
 
 def device_error(device=None) -> int:

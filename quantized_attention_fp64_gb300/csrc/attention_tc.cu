@@ -71,12 +71,14 @@ constexpr int kBarVFull = kBarKEmpty + kKStages, kBarVEmpty = kBarVFull + kVStag
 constexpr int kBarSFull = kBarVEmpty + kVStages, kBarSFree = kBarSFull + 2;
 constexpr int kBarPFull = kBarSFree + 2, kBarPVDone = kBarPFull + 2;
 constexpr int kBarOEmpty = kBarPVDone + 2, kBarDrain = kBarOEmpty + 2;
-constexpr int kNumBars = kBarDrain + 2;
+constexpr int kBarVs = kBarDrain + 2;  // a softmax warpgroup's V scales are parked
+constexpr int kNumBars = kBarVs + 2;
 template <int D>
 struct SmemTail {
   static constexpr uint32_t kOffTmemSlot = Smem<D>::kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffAbort = kOffTmemSlot + 8;
-  static constexpr uint32_t kBytes = kOffAbort + 8 + 1024;  // + alignment slack
+  static constexpr uint32_t kOffVs = (kOffAbort + 8 + 15) / 16 * 16;  // [warpgroup][unit parity][D] fp32
+  static constexpr uint32_t kBytes = kOffVs + 4 * D * 4 + 1024;      // + alignment slack
 };
 
 // TMEM columns: S of query tile i at 128*i, O of query tile i (D columns) at 256 + D*i
@@ -353,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(cx.bar(kBarPVDone + s), 1);
       tc::mbar_init(cx.bar(kBarOEmpty + s), 128);
       tc::mbar_init(cx.bar(kBarDrain + s), 1);
+      tc::mbar_init(cx.bar(kBarVs + s), 128);
     }
     tc::fence_mbar_init();
   }
@@ -369,6 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + T::kOffTmemSlot);
+  // launched as a programmatic dependent: the previous kernel of the stream
+  // (which writes the bundle, or reads the output buffer) must be complete
+  // before any global memory is touched
+  tc::griddep_wait();
 
   if (warp < 4) {
     // control warpgroup: one register decrease for all four warps
@@ -515,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_addr + col_o<D>(i);
     uint8_t* p_row = smem + L::kOffP + static_cast<uint32_t>(i) * kTile8 + row * 128;
     const int64_t nblk = prm.S_pad / kQKBlock;
-    uint32_t s_cnt = 0, pv_cnt = 0;
+    uint32_t s_cnt = 0, pv_cnt = 0, vs_cnt = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < prm.n_units; u += gridDim.x) {
       const int64_t bh = u / prm.pairs_per_head;
@@ -523,6 +530,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_valid = qrow < prm.S;
       const float cq = row_valid ? prm.q_scale[bh * nblk + qrow / kQKBlock] * prm.sm_log2 : 0.0f;
       const float* ks = prm.k_scale + bh * nblk;
+      // the V scale of channel `row` (the first D threads) is copied into
+      // shared memory now, asynchronously, for the epilogue (double-buffered
+      // by unit: every thread of the warpgroup has finished the epilogue
+      // two units back before this thread passes the previous unit's wait)
+      float* vs_buf = reinterpret_cast<float*>(smem + T::kOffVs) + (2 * i + (vs_cnt & 1u)) * D;
+      if (row < D) tc::cp_async4(tc::smem_u32(vs_buf + row), prm.v_scale + bh * D + row);
       float m = -INFINITY, l = 0.0f;
       float cb[4];
       // K scales of a 128-key tile: 4 consecutive floats, 16-byte aligned
@@ -560,8 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // epilogue: the last PV of the unit completes O; O = acc * s_v / l (l
       // counts p448), bf16 in the output layout
+      tc::cp_async_wait_all();
+      tc::mbar_arrive(cx.bar(kBarVs + i));
       if (!(ok = wait_bar_warp(cx, cx.bar(kBarPVDone + i), pv_cnt & 1u))) break;
       ++pv_cnt;
+      if (!(ok = wait_bar_warp(cx, cx.bar(kBarVs + i), vs_cnt & 1u))) break;
+      ++vs_cnt;
       tc::tc_fence_after();
       const float inv_l = 1.0f / l;
       if (prm.lse != nullptr && row_valid) {
@@ -569,28 +586,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         // logits in base 2, l counting 448 * 2^(x - m)
         prm.lse[bh * prm.S + qrow] = (m + log2f(l) - kLog2P) * kLn2;
       }
-      const float* sv = prm.v_scale + bh * D;
+      // Each warp writes its 32 rows through its 4 KB of this warpgroup's P
+      // tile (free once the last PV is done): a lane parks its row's 64
+      // bytes of a 32-channel slice, then each store instruction covers 8
+      // rows x 64 contiguous bytes instead of 32 rows x 16 bytes. The 16-byte
+      // chunk q of staged row r sits at slot (q + r / 2) & 3, so that both
+      // the parking and the reading are free of bank conflicts.
       const int64_t b_idx = bh / prm.H, h_idx = bh % prm.H;
-      uint16_t* dst = prm.out.p + b_idx * prm.out.sb + qrow * prm.out.ss + h_idx * prm.out.sh;
+      const int64_t row0 = qrow - lane;  // this warp's first row
+      uint8_t* stage = smem + L::kOffP + static_cast<uint32_t>(i) * kTile8 + static_cast<uint32_t>(wq) * 4096u;
+      const int rr = lane >> 2, qq = lane & 3;  // the row (of 8) and chunk this lane stores
+      uint16_t* dst[4];
+      bool dst_ok[4];
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm) {
+        const int64_t r = row0 + 8 * mm + rr;
+        dst_ok[mm] = r < prm.S;
+        dst[mm] = prm.out.p + b_idx * prm.out.sb + r * prm.out.ss + h_idx * prm.out.sh + 8 * qq;
+      }
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tc::tmem_ld32(tO + 32u * c, o);
         tc::tmem_wait_ld();
-        if (row_valid) {
-          uint32_t pk[16];
+        uint32_t pk[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 s2 = __ldg(reinterpret_cast<const float2*>(sv + 32 * c + 2 * k));
-            const float a0 = __uint_as_float(o[2 * k]) * inv_l * s2.x;
-            const float a1 = __uint_as_float(o[2 * k + 1]) * inv_l * s2.y;
-            const __nv_bfloat162 v2 = __floats2bfloat162_rn(a0, a1);
-            pk[k] = *reinterpret_cast<const uint32_t*>(&v2);
-          }
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        for (int k = 0; k < 16; ++k) {
+          const float2 s2 = *reinterpret_cast<const float2*>(vs_buf + 32 * c + 2 * k);
+          const float a0 = __uint_as_float(o[2 * k]) * inv_l * s2.x;
+          const float a1 = __uint_as_float(o[2 * k + 1]) * inv_l * s2.y;
+          const __nv_bfloat162 v2 = __floats2bfloat162_rn(a0, a1);
+          pk[k] = *reinterpret_cast<const uint32_t*>(&v2);
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(stage + lane * 64 + ((q + (lane >> 1)) & 3) * 16) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+          const int r = 8 * mm + rr;
+          const uint4 val = *reinterpret_cast<const uint4*>(stage + r * 64 + ((qq + (r >> 1)) & 3) * 16);
+          if (dst_ok[mm]) *reinterpret_cast<uint4*>(dst[mm] + 32 * c) = val;
+        }
+        __syncwarp();
       }
       tc::tc_fence_before();
       tc::mbar_arrive(cx.bar(kBarOEmpty + i));
@@ -649,13 +688,24 @@ cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t 
   auto kernel = D == 128 ? (causal ? attention_tc_kernel<128, true> : attention_tc_kernel<128, false>)
                          : (causal ? attention_tc_kernel<64, true> : attention_tc_kernel<64, false>);
   const uint32_t smem_bytes = D == 128 ? SmemTail<128>::kBytes : SmemTail<64>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem_bytes));
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kernel), static_cast<int>(smem_bytes));
   if (e != cudaSuccess) return e;
   const int sms = sm_count_current();
   const int grid = static_cast<int>(p.n_units < sms ? p.n_units : sms);
-  kernel<<<grid, kThreads, smem_bytes, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs may start (barriers, TMEM,
+  // tensor maps) while the previous kernel of the stream, normally the
+  // prologue, still runs; they wait for it before reading anything
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
 }
 
 }  // namespace sage

@@ -455,6 +455,145 @@ __device__ __forceinline__ bool v_code_quad_fast(uint2 w, float2 r01, float2 r23
   return cd == cu;
 }
 
+// Exact fp64 sums of one 32-token key chunk, by the two warps of a pair
+// (sub 0 and 1, 16 rows each; rows: this warp's rows, read with 8-channel
+// lanes; nv: its rows below S; nvc: the chunk's rows below S). The second
+// half posts its float pairs and magnitude bounds in xk_*; the first half
+// joins them, replaces the result by the left-to-right fp64 sums when the
+// pair sums may be inexact, and writes the chunk's 128 sums to ks_chunk.
+// `release` runs once the warp has stopped reading its rows.
+template <typename Release>
+__device__ __forceinline__ void key_chunk_sums(const uint8_t* rows, int nv, int nvc, int sub, int lane, int pair,
+                                               float* xk_hi, float* xk_lo, uint32_t* xk_bits, double* ks_chunk,
+                                               Release release) {
+  float2 hi[4], lo[4];
+  uint32_t mx, mn;
+  if (nv == kHalfRows)
+    key_sum_partial<true>(rows, kHalfRows, lane, hi, lo, mx, mn);
+  else
+    key_sum_partial<false>(rows, nv, lane, hi, lo, mx, mn);
+  if (sub == 1) {
+    if (lane < 16) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        xk_hi[8 * lane + 2 * k] = hi[k].x;
+        xk_hi[8 * lane + 2 * k + 1] = hi[k].y;
+        xk_lo[8 * lane + 2 * k] = lo[k].x;
+        xk_lo[8 * lane + 2 * k + 1] = lo[k].y;
+      }
+    }
+    if (lane == 0) {
+      xk_bits[0] = mx;
+      xk_bits[1] = mn;
+    }
+    pair_bar(pair);
+    release();
+    return;
+  }
+  pair_bar(pair);
+  const int cb = 8 * (lane & 15);
+  double sums[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float2 s, e;
+    two_sum2(hi[k], make_float2(xk_hi[cb + 2 * k], xk_hi[cb + 2 * k + 1]), s, e);
+    const float2 l = __fadd2_rn(__fadd2_rn(lo[k], make_float2(xk_lo[cb + 2 * k], xk_lo[cb + 2 * k + 1])), e);
+    sums[2 * k] = __dadd_rn(static_cast<double>(s.x), static_cast<double>(l.x));
+    sums[2 * k + 1] = __dadd_rn(static_cast<double>(s.y), static_cast<double>(l.y));
+  }
+  if (!key_sum_exact(__vmaxu2(mx, xk_bits[0]), __vminu2(mn, xk_bits[1]))) {
+    // this warp's rows are followed by the second half's in the tile
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) sums[c] = fp64_chunk_sum(rows, nvc, (lane & 15) * 16 + 2 * c);
+  }
+  release();
+  if (lane < 16) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) ks_chunk[cb + c] = sums[c];
+  }
+}
+
+// Max |v| of one warp's 16 V rows per channel, as bf16 magnitude bits (they
+// order as integers): on return m4[k] holds channels (8l+2k, 8l+2k+1), l =
+// lane & 15, in its low and high halves, over the rows of this half-warp
+// (tokens of parity lane >> 4); the caller joins the two half-warps.
+__device__ __forceinline__ void v_max_rows(const uint8_t* vr, int nv, int lane, uint32_t (&m4)[4]) {
+  const int half = lane >> 4;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m4[k] = 0u;
+  if (nv == kHalfRows) {
+#pragma unroll
+    for (int i = 0; i < kHalfRows / 4; ++i) {
+      const uint4 wa = tok8(vr, 4 * i + half, lane), wb = tok8(vr, 4 * i + 2 + half, lane);
+      m4[0] = __vimax3_u16x2(m4[0], wa.x & kAbs2, wb.x & kAbs2);
+      m4[1] = __vimax3_u16x2(m4[1], wa.y & kAbs2, wb.y & kAbs2);
+      m4[2] = __vimax3_u16x2(m4[2], wa.z & kAbs2, wb.z & kAbs2);
+      m4[3] = __vimax3_u16x2(m4[3], wa.w & kAbs2, wb.w & kAbs2);
+    }
+  } else {
+    for (int i = 0; i < kHalfRows / 2; ++i) {
+      const int t = 2 * i + half;
+      if (t < nv) {
+        const uint4 w = tok8(vr, t, lane);
+        m4[0] = __vmaxu2(m4[0], w.x & kAbs2);
+        m4[1] = __vmaxu2(m4[1], w.y & kAbs2);
+        m4[2] = __vmaxu2(m4[2], w.z & kAbs2);
+        m4[3] = __vmaxu2(m4[3], w.w & kAbs2);
+      }
+    }
+  }
+}
+
+// e4m3 codes of one warp's 16 V rows (4-channel lanes: channels 4*lane ..
+// +4, scales svs), written transposed: 16 tokens of channel 4*lane+c at
+// vt_bh[(4*lane+c) * S_pad + s0]. Rows at or past nv get code 0. `release`
+// runs once the warp has stopped reading its rows.
+template <typename Release>
+__device__ __forceinline__ void v_codes_rows(const uint8_t* rows, int nv, int lane, float4 svs, uint8_t* vt_bh,
+                                             int64_t S_pad, int64_t s0, Release release) {
+  const float sc[4] = {svs.x, svs.y, svs.z, svs.w};
+  float rv[4];
+  uint32_t keep = 0u;
+  bool fast = true;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    rv[c] = sc[c] >= FLT_MIN ? __frcp_rn(sc[c]) : 0.0f;
+    if (sc[c] > 0.0f) keep |= 0xFFu << (8 * c);
+    fast = fast && (sc[c] >= FLT_MIN || sc[c] == 0.0f);  // zero channels are masked to code 0
+  }
+  const float2 r01 = make_float2(rv[0], rv[1]), r23 = make_float2(rv[2], rv[3]);
+  uint32_t a[kHalfRows];  // a[t]: the 4 channels' codes of token t
+  uint32_t redo = 0u;     // bit t: token t needs the exact division
+#pragma unroll
+  for (int t = 0; t < kHalfRows; ++t) {
+    a[t] = 0u;
+    if (nv == kHalfRows || t < nv) {
+      uint32_t code;
+      if (!(v_code_quad_fast(tok4(rows, t, lane), r01, r23, code) && fast)) redo |= 1u << t;
+      a[t] = code & keep;
+    }
+  }
+  if (redo != 0u) {
+    // rare: tokens whose fast codes are not certain
+#pragma unroll
+    for (int t = 0; t < kHalfRows; ++t)
+      if ((redo >> t) & 1u) a[t] = exact_v_quad(tok4(rows, t, lane), svs) & keep;
+  }
+  release();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    // 4x4 byte transposes: tokens 4j..4j+3 of channel 4*lane+c
+    uint32_t cw[4];
+#pragma unroll
+    for (int j = 0; j < kHalfRows / 4; ++j) {
+      const uint32_t lo01 = __byte_perm(a[4 * j], a[4 * j + 1], (c & 2) ? 0x7362 : 0x5140);
+      const uint32_t lo23 = __byte_perm(a[4 * j + 2], a[4 * j + 3], (c & 2) ? 0x7362 : 0x5140);
+      cw[j] = __byte_perm(lo01, lo23, (c & 1) ? 0x7632 : 0x5410);
+    }
+    __stcs(reinterpret_cast<uint4*>(vt_bh + (4 * lane + c) * S_pad + s0), make_uint4(cw[0], cw[1], cw[2], cw[3]));
+  }
+}
+
 // Pairwise tree (padded with +0.0 to a power of two) over `n` group sums
 // starting at p, stride 128 doubles, evaluated streaming: stack[l] holds a
 // finished subtree of 2^l leaves. Aligned blocks of 16 leaves are loaded
@@ -597,6 +736,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float xa[2][kTeams * kWarps / 2][2];     // amax of each half block, two parities
   __shared__ float fin_vmax[kHeadDim];
   __shared__ double fin_right[kHeadDim];
+  // the next kernel of the stream (the attention kernel, launched as a
+  // programmatic dependent) may be scheduled once every CTA of this grid has
+  // started; it waits for this grid to end before it reads anything
+  tc::griddep_launch_dependents();
   const uint32_t sbase = tc::smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t* meta_item = reinterpret_cast<int64_t*>(smem + kOffMeta);             // [kStages]
@@ -885,82 +1028,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (prm.smooth_k) {
         // K tile: exact fp64 chunk sums, the second half's partial sums
         // joined into the first half's
-        const uint8_t* rows = stage_rows(c2);
-        float2 hi[4], lo[4];
-        uint32_t mx, mn;
-        if (nv == kHalfRows)
-          key_sum_partial<true>(rows, kHalfRows, lane, hi, lo, mx, mn);
-        else
-          key_sum_partial<false>(rows, nv, lane, hi, lo, mx, mn);
-        if (sub == 1) {
-          if (lane < 16) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              xk_hi[chunk][8 * lane + 2 * k] = hi[k].x;
-              xk_hi[chunk][8 * lane + 2 * k + 1] = hi[k].y;
-              xk_lo[chunk][8 * lane + 2 * k] = lo[k].x;
-              xk_lo[chunk][8 * lane + 2 * k + 1] = lo[k].y;
-            }
-          }
-          if (lane == 0) {
-            xk_bits[chunk][0] = mx;
-            xk_bits[chunk][1] = mn;
-          }
-          pair_bar(pair);
-          tc::mbar_arrive(cx.empty(c2 % kStages));
-        } else {
-          pair_bar(pair);
-          const int cb = 8 * (lane & 15);
-          double sums[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float2 s, e;
-            two_sum2(hi[k], make_float2(xk_hi[chunk][cb + 2 * k], xk_hi[chunk][cb + 2 * k + 1]), s, e);
-            const float2 l = __fadd2_rn(
-                __fadd2_rn(lo[k], make_float2(xk_lo[chunk][cb + 2 * k], xk_lo[chunk][cb + 2 * k + 1])), e);
-            sums[2 * k] = __dadd_rn(static_cast<double>(s.x), static_cast<double>(l.x));
-            sums[2 * k + 1] = __dadd_rn(static_cast<double>(s.y), static_cast<double>(l.y));
-          }
-          if (!key_sum_exact(__vmaxu2(mx, xk_bits[chunk][0]), __vminu2(mn, xk_bits[chunk][1]))) {
-            // this warp's rows are followed by the second half's in the tile
-            const int nvc = valid_rows(S, s0c, kQKBlock);
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) sums[c] = fp64_chunk_sum(rows, nvc, (lane & 15) * 16 + 2 * c);
-          }
-          tc::mbar_arrive(cx.empty(c2 % kStages));
-          if (lane < 16) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) ks[chunk][cb + c] = sums[c];
-          }
-        }
+        const uint32_t ks_stage = c2 % kStages;
+        key_chunk_sums(stage_rows(c2), nv, valid_rows(S, s0c, kQKBlock), sub, lane, pair, xk_hi[chunk],
+                       xk_lo[chunk], xk_bits[chunk], ks[chunk], [&]() { tc::mbar_arrive(cx.empty(ks_stage)); });
         ++c2;
         if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
       }
       // V tile: max |v| per channel (bf16 magnitudes compare as integers)
-      const uint8_t* vr = stage_rows(c2);
-      const int half = lane >> 4;
-      uint32_t m4[4] = {0u, 0u, 0u, 0u};  // channel pairs (8l, 8l+1) .. (8l+6, 8l+7)
-      if (nv == kHalfRows) {
-#pragma unroll
-        for (int i = 0; i < kHalfRows / 4; ++i) {
-          const uint4 wa = tok8(vr, 4 * i + half, lane), wb = tok8(vr, 4 * i + 2 + half, lane);
-          m4[0] = __vimax3_u16x2(m4[0], wa.x & kAbs2, wb.x & kAbs2);
-          m4[1] = __vimax3_u16x2(m4[1], wa.y & kAbs2, wb.y & kAbs2);
-          m4[2] = __vimax3_u16x2(m4[2], wa.z & kAbs2, wb.z & kAbs2);
-          m4[3] = __vimax3_u16x2(m4[3], wa.w & kAbs2, wb.w & kAbs2);
-        }
-      } else {
-        for (int i = 0; i < kHalfRows / 2; ++i) {
-          const int t = 2 * i + half;
-          if (t < nv) {
-            const uint4 w = tok8(vr, t, lane);
-            m4[0] = __vmaxu2(m4[0], w.x & kAbs2);
-            m4[1] = __vmaxu2(m4[1], w.y & kAbs2);
-            m4[2] = __vmaxu2(m4[2], w.z & kAbs2);
-            m4[3] = __vmaxu2(m4[3], w.w & kAbs2);
-          }
-        }
-      }
+      uint32_t m4[4];  // channel pairs (8l, 8l+1) .. (8l+6, 8l+7)
+      v_max_rows(stage_rows(c2), nv, lane, m4);
       tc::mbar_arrive(cx.empty(c2 % kStages));
 #pragma unroll
       for (int k = 0; k < 4; ++k) m4[k] = __vmaxu2(m4[k], __shfl_xor_sync(0xffffffffu, m4[k], 16));
@@ -1000,49 +1076,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_arrive(cx.empty(st));  // the K tile is team 1's
       const uint32_t c2 = cnt + 1;
       if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
-      const uint8_t* rows = stage_rows(c2);
-      const float sc[4] = {svs.x, svs.y, svs.z, svs.w};
-      float rv[4];
-      uint32_t keep = 0u;
-      bool fast = true;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        rv[c] = sc[c] >= FLT_MIN ? __frcp_rn(sc[c]) : 0.0f;
-        if (sc[c] > 0.0f) keep |= 0xFFu << (8 * c);
-        fast = fast && (sc[c] >= FLT_MIN || sc[c] == 0.0f);  // zero channels are masked to code 0
-      }
-      const float2 r01 = make_float2(rv[0], rv[1]), r23 = make_float2(rv[2], rv[3]);
-      uint32_t a[kHalfRows];  // a[t]: the 4 channels' codes of token t
-      uint32_t redo = 0u;     // bit t: token t needs the exact division
-#pragma unroll
-      for (int t = 0; t < kHalfRows; ++t) {
-        a[t] = 0u;
-        if (nv == kHalfRows || t < nv) {
-          uint32_t code;
-          if (!(v_code_quad_fast(tok4(rows, t, lane), r01, r23, code) && fast)) redo |= 1u << t;
-          a[t] = code & keep;
-        }
-      }
-      if (redo != 0u) {
-        // rare: tokens whose fast codes are not certain
-#pragma unroll
-        for (int t = 0; t < kHalfRows; ++t)
-          if ((redo >> t) & 1u) a[t] = exact_v_quad(tok4(rows, t, lane), svs) & keep;
-      }
-      tc::mbar_arrive(cx.empty(c2 % kStages));
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        // 4x4 byte transposes: tokens 4j..4j+3 of channel 4*lane+c
-        uint32_t cw[4];
-#pragma unroll
-        for (int j = 0; j < kHalfRows / 4; ++j) {
-          const uint32_t lo01 = __byte_perm(a[4 * j], a[4 * j + 1], (c & 2) ? 0x7362 : 0x5140);
-          const uint32_t lo23 = __byte_perm(a[4 * j + 2], a[4 * j + 3], (c & 2) ? 0x7362 : 0x5140);
-          cw[j] = __byte_perm(lo01, lo23, (c & 1) ? 0x7632 : 0x5410);
-        }
-        __stcs(reinterpret_cast<uint4*>(prm.out.vt_codes + (bh * kHeadDim + 4 * lane + c) * S_pad + s0),
-               make_uint4(cw[0], cw[1], cw[2], cw[3]));
-      }
+      const uint32_t v_stage = c2 % kStages;
+      v_codes_rows(stage_rows(c2), nv, lane, svs, prm.out.vt_codes + bh * kHeadDim * S_pad, S_pad, s0,
+                   [&]() { tc::mbar_arrive(cx.empty(v_stage)); });
     } else {
       // codes item, team 1: K codes of k - mean; the key mean comes with the
       // K tile
@@ -1070,6 +1106,215 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!pass(cnt + 1)) break;
     }
     cnt += n_stages;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Short sequences: one cluster of G = ceil(S / 128) <= kShortMaxGroups CTAs
+// per (batch, head). CTA g holds group g (tokens 128g .. 128g+127) of the
+// head's Q, K and V in shared memory, one TMA copy each, and writes every
+// output of that group. Two teams of 8 warps split the work so that the
+// chain each warp runs stays short (short calls wait for it): team 0 takes
+// the V maxima, codes Q while the group results are exchanged, then codes V;
+// team 1 sums K, exchanges the results, finishes the head's statistics and
+// codes K. Each CTA stores its group's key sums and V maxima
+// into the shared memory of every CTA of the cluster; after one cluster
+// barrier all of them hold every group's results, so the prologue is a
+// single launch with no global counters and no scratch, and each input byte
+// is read once. The arithmetic is the persistent kernel's (the same per-warp
+// helpers; the same pairwise tree over the group sums, padded with +0.0 to a
+// power of two, where padding changes nothing), so the outputs are
+// identical.
+constexpr int kShortMaxGroups = 8;                 // the portable cluster size
+constexpr int kShortThreads = kTeams * kTeamThreads;
+constexpr uint32_t kShortSmemBytes = 3 * kTileBytes + 128;  // Q, K, V tiles + alignment slack
+
+__global__ void __launch_bounds__(kShortThreads, 1)
+    prologue_short_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const Params prm, int3 s_axis) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ double ks[kChunks][kHeadDim];       // exact chunk sums of this group
+  __shared__ uint32_t vm[kWarps][kHeadDim / 2];  // per-warp max |v| bits, channel pairs
+  __shared__ float xk_hi[kChunks][kHeadDim], xk_lo[kChunks][kHeadDim];  // second-half key sums
+  __shared__ uint32_t xk_bits[kChunks][2];       // second-half magnitude bounds
+  __shared__ float xa[kTeams * kWarps / 2][2];   // block amax exchange of each warp pair
+  __shared__ double g_sum[kShortMaxGroups][kHeadDim];    // every group's key sums (stored by the cluster)
+  __shared__ uint32_t g_max[kShortMaxGroups][kHeadDim];  // every group's max |v| bits
+  __shared__ __align__(16) float h_mean[kHeadDim];
+  __shared__ __align__(16) float h_vscale[kHeadDim];
+  __shared__ __align__(8) uint64_t bars[3];      // Q, K, V tile full
+  __shared__ int abort_flag;
+
+  // the next kernel of the stream (the attention kernel, launched as a
+  // programmatic dependent) may be scheduled now; it waits for this grid
+  tc::griddep_launch_dependents();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tt = threadIdx.x;
+  const int64_t G = prm.G, S = prm.S, S_pad = prm.S_pad, nblk = S_pad / kQKBlock;
+  const int g = static_cast<int>(tc::cluster_ctarank());
+  const int64_t bh = static_cast<int64_t>(blockIdx.x) / G;
+  const int64_t b = bh / prm.H, h = bh % prm.H;
+  const uint32_t sbase = tc::smem_u32(smem);
+  Ctx cx;
+  cx.bar0 = tc::smem_u32(bars);
+  cx.abort_flag = &abort_flag;
+  cx.dev_err = prm.dev_err;
+  if (tt == 0) {
+    abort_flag = 0;
+    for (int n = 0; n < 3; ++n) tc::mbar_init(cx.full(n), 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  // first half of the barrier that makes sure every CTA of the cluster runs
+  // before any of them stores into another's shared memory
+  tc::cluster_arrive_relaxed();
+  const int64_t s_group = static_cast<int64_t>(g) * kItemTokens;
+  if (tt == 0) {
+    const uint64_t pol = tc::policy_evict_first();  // every tile is read once
+    const CUtensorMap* maps[3] = {&tm_q, &tm_k, &tm_v};
+    const int axes[3] = {s_axis.x, s_axis.y, s_axis.z};
+    const int32_t sc = static_cast<int32_t>(s_group), hc = static_cast<int32_t>(h), bc = static_cast<int32_t>(b);
+#pragma unroll
+    for (int n = 0; n < 3; ++n) {
+      tc::mbar_arrive_expect_tx(cx.full(n), kTileBytes);
+      if (axes[n] == 1)
+        tc::tma_load_4d_hint(sbase + n * kTileBytes, maps[n], 0, sc, hc, bc, cx.full(n), pol);
+      else
+        tc::tma_load_4d_hint(sbase + n * kTileBytes, maps[n], 0, hc, sc, bc, cx.full(n), pol);
+    }
+  }
+
+  // In each team warps 2c and 2c+1 take the two halves (16 tokens each) of
+  // chunk c. A failed wait is recorded (error word) but changes no control
+  // flow: every thread reaches every barrier below, the cluster's included.
+  // Named barriers: 1, team 0's V maxima to team 1 (team 0 arrives, team 1
+  // waits); 2, the head's scales from team 1 to team 0; 11, within team 1;
+  // 3..10, the warp pairs.
+  const int team = warp / kWarps, tw = warp % kWarps, chunk = tw >> 1, sub = tw & 1, pair = warp >> 1;
+  const int64_t s0c = s_group + chunk * kQKBlock, s0 = s0c + sub * kHalfRows;
+  const int nv = valid_rows(S, s0, kHalfRows);
+  const uint32_t row_off = static_cast<uint32_t>(tw * kHalfRows * 256);
+  const uint8_t* q_rows = smem + row_off;
+  const uint8_t* k_rows = smem + kTileBytes + row_off;
+  const uint8_t* v_rows = smem + 2 * kTileBytes + row_off;
+  bool ok = true;
+  if (team == 0) {
+    // the group's max |v| per channel, handed to team 1
+    ok = wait_bar(cx, cx.full(2), 0);
+    uint32_t m4[4];
+    v_max_rows(v_rows, nv, lane, m4);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m4[k] = __vmaxu2(m4[k], __shfl_xor_sync(0xffffffffu, m4[k], 16));
+    if (lane < 16) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) vm[tw][4 * lane + k] = m4[k];
+    }
+    asm volatile("bar.arrive 1, %0;" ::"n"(kShortThreads) : "memory");
+    // team 0 stores nothing into other CTAs: it passes the cluster's
+    // barriers at once and codes Q while the group results are exchanged
+    tc::cluster_wait_acquire();
+    tc::cluster_arrive_relaxed();
+    ok = wait_bar(cx, cx.full(0), 0) && ok;
+    const float2 nz[4] = {};
+    int8_t* qc = prm.write_int8 ? prm.out.q_codes + bh * S_pad * kHeadDim : nullptr;
+    uint16_t* q16 = prm.out.q16 + bh * S_pad * kHeadDim;
+    const float s = nv == kHalfRows ? quantize_half_block<false, true>(q_rows, nz, kHalfRows, qc, q16, s0, lane,
+                                                                       &xa[pair][sub], &xa[pair][sub ^ 1], pair)
+                                    : quantize_half_block<false, false>(q_rows, nz, nv, qc, q16, s0, lane,
+                                                                        &xa[pair][sub], &xa[pair][sub ^ 1], pair);
+    if (sub == 0 && lane == 0) prm.out.q_scale[bh * nblk + s0c / kQKBlock] = s;
+    tc::cluster_wait_acquire();
+    asm volatile("bar.sync 2, %0;" ::"n"(kShortThreads) : "memory");  // the V scales are in h_vscale
+    // V codes, transposed (4-channel lanes)
+    v_codes_rows(v_rows, nv, lane, *reinterpret_cast<const float4*>(h_vscale + 4 * lane),
+                 prm.out.vt_codes + bh * kHeadDim * S_pad, S_pad, s0, [] {});
+  } else {
+    // the group's exact key sums
+    ok = wait_bar(cx, cx.full(1), 0);
+    if (prm.smooth_k)
+      key_chunk_sums(k_rows, nv, valid_rows(S, s0c, kQKBlock), sub, lane, pair, xk_hi[chunk], xk_lo[chunk],
+                     xk_bits[chunk], ks[chunk], [] {});
+    asm volatile("bar.sync 1, %0;" ::"n"(kShortThreads) : "memory");  // team 0's V maxima are in vm
+    tc::cluster_wait_acquire();  // every CTA of the cluster has started
+    const int c = tt - kTeamThreads;
+    if (c < kHeadDim) {
+      // the group's results: levels 1 and 2 of the pairwise tree over its 4
+      // chunk sums, and its max |v| per channel, stored into slot g of every
+      // CTA of the cluster (this one included)
+      const double gs =
+          prm.smooth_k ? __dadd_rn(__dadd_rn(ks[0][c], ks[1][c]), __dadd_rn(ks[2][c], ks[3][c])) : 0.0;
+      uint32_t mb = 0u;
+#pragma unroll
+      for (int i = 0; i < kWarps; ++i) {
+        const uint32_t pr = vm[i][c >> 1];
+        mb = max(mb, (c & 1) ? (pr >> 16) : (pr & 0xFFFFu));
+      }
+      const uint32_t a_sum = tc::smem_u32(&g_sum[g][c]), a_max = tc::smem_u32(&g_max[g][c]);
+      for (int r = 0; r < G; ++r) {
+        tc::st_cluster_f64(tc::mapa_shared(a_sum, static_cast<uint32_t>(r)), gs);
+        tc::st_cluster_u32(tc::mapa_shared(a_max, static_cast<uint32_t>(r)), mb);
+      }
+    }
+    // every group's results are in every CTA's shared memory; after this
+    // barrier no CTA touches another's shared memory, so each may exit freely
+    tc::cluster_arrive_release();
+    tc::cluster_wait_acquire();
+    if (c < kHeadDim) {
+      // the head's key mean and V scale of channel c (the same in every CTA):
+      // the pairwise tree over the P = 2^ceil(log2 G) group sums
+      double lv[kShortMaxGroups];
+      float vmx = 0.0f;
+#pragma unroll
+      for (int r = 0; r < kShortMaxGroups; ++r) {
+        lv[r] = r < G ? g_sum[r][c] : 0.0;
+        if (r < G) vmx = fmaxf(vmx, __uint_as_float(g_max[r][c] << 16));
+      }
+#pragma unroll
+      for (int w = 1; w < kShortMaxGroups; w *= 2) {
+        if (w >= G) break;  // lv[0] already holds the tree of the first P leaves
+#pragma unroll
+        for (int k = 0; k < kShortMaxGroups; k += 2 * w) lv[k] = __dadd_rn(lv[k], lv[k + w]);
+      }
+      const float mu = prm.smooth_k ? __double2float_rn(__ddiv_rn(lv[0], static_cast<double>(S))) : 0.0f;
+      const float vs = __fdiv_rn(vmx, kE4M3Max);
+      h_mean[c] = mu;
+      h_vscale[c] = vs;
+      if (g == 0) {
+        prm.out.k_mean[bh * kHeadDim + c] = mu;
+        prm.out.v_scale[bh * kHeadDim + c] = vs;
+      }
+    }
+    asm volatile("bar.arrive 2, %0;" ::"n"(kShortThreads) : "memory");  // h_vscale to team 0
+    asm volatile("bar.sync 11, %0;" ::"n"(kTeamThreads) : "memory");    // h_mean within team 1
+    // K codes of k - mean
+    int8_t* kc = prm.write_int8 ? prm.out.k_codes + bh * S_pad * kHeadDim : nullptr;
+    uint16_t* k16 = prm.out.k16 + bh * S_pad * kHeadDim;
+    float skv;
+    if (prm.smooth_k) {
+      const float4* mp = reinterpret_cast<const float4*>(h_mean + 8 * (lane & 15));
+      const float4 ma = mp[0], mb = mp[1];
+      const float2 nmu[4] = {make_float2(-ma.x, -ma.y), make_float2(-ma.z, -ma.w), make_float2(-mb.x, -mb.y),
+                             make_float2(-mb.z, -mb.w)};
+      skv = nv == kHalfRows ? quantize_half_block<true, true>(k_rows, nmu, kHalfRows, kc, k16, s0, lane,
+                                                              &xa[pair][sub], &xa[pair][sub ^ 1], pair)
+                            : quantize_half_block<true, false>(k_rows, nmu, nv, kc, k16, s0, lane, &xa[pair][sub],
+                                                               &xa[pair][sub ^ 1], pair);
+    } else {
+      const float2 nz[4] = {};
+      skv = nv == kHalfRows ? quantize_half_block<false, true>(k_rows, nz, kHalfRows, kc, k16, s0, lane,
+                                                               &xa[pair][sub], &xa[pair][sub ^ 1], pair)
+                            : quantize_half_block<false, false>(k_rows, nz, nv, kc, k16, s0, lane, &xa[pair][sub],
+                                                                &xa[pair][sub ^ 1], pair);
+    }
+    if (sub == 0 && lane == 0) prm.out.k_scale[bh * nblk + s0c / kQKBlock] = skv;
+  }
+  if (!ok) {
+    // let every copy land before the CTA exits
+    Ctx drain = cx;
+    volatile int no_abort = 0;
+    drain.abort_flag = &no_abort;
+    for (int n = 0; n < 3; ++n) wait_bar(drain, cx.full(n), 0);
   }
 }
 
@@ -1147,13 +1392,34 @@ cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, i
   const int aq = make_input_map(&tq, q, B, S, H), ak = make_input_map(&tk, k, B, S, H),
             av = make_input_map(&tv, v, B, S, H);
   if (aq == 0 || ak == 0 || av == 0) return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(scratch, 0, l.header, stream);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return e;
+  const int3 axes = make_int3(aq, ak, av);
+  cudaError_t e;
+  if (p.G <= kShortMaxGroups) {
+    // short sequences: one cluster per head, no scratch
+    if ((e = set_smem_limit_once(reinterpret_cast<const void*>(prologue_short_kernel),
+                                 static_cast<int>(kShortSmemBytes))) != cudaSuccess)
+      return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.G * p.NH));
+    cfg.blockDim = dim3(kShortThreads);
+    cfg.dynamicSmemBytes = kShortSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.G);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prologue_short_kernel, tq, tk, tv, p, axes);
+  }
+  if ((e = cudaMemsetAsync(scratch, 0, l.header, stream)) != cudaSuccess) return e;
+  if ((e = set_smem_limit_once(reinterpret_cast<const void*>(prologue_kernel), static_cast<int>(kSmemBytes))) !=
+      cudaSuccess)
+    return e;
   const int sms = sm_count_current();
   const int grid = static_cast<int>(p.total < sms ? p.total : sms);
-  prologue_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p, make_int3(aq, ak, av));
+  prologue_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p, axes);
   return cudaGetLastError();
 }
 

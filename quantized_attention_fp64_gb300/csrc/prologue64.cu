@@ -24,6 +24,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace sage {
 namespace {
@@ -156,6 +157,9 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {  // high byte = c
 }
 
 __global__ void __launch_bounds__(kWarps * 32) p64_codes(const P64 p) {
+  // the attention kernel after it is a programmatic dependent: it may be
+  // scheduled now and waits for this grid to end before it reads anything
+  tc::griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t b = blockIdx.z, h = blockIdx.y, bh = b * p.H + h;
   const int64_t c = static_cast<int64_t>(blockIdx.x) * kWarps + warp;

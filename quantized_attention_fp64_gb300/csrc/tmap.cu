@@ -42,6 +42,25 @@ bool make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+cudaError_t set_smem_limit_once(const void* func, int bytes) {
+  struct Entry {
+    const void* func;
+    int dev, bytes;
+  };
+  static std::mutex mu;
+  static Entry seen[128];
+  static int n_seen = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_seen; ++i)
+    if (seen[i].func == func && seen[i].dev == dev && seen[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && n_seen < 128) seen[n_seen++] = Entry{func, dev, bytes};
+  return e;
+}
+
 int sm_count_current() {
   static int counts[64] = {};
   int dev = 0;
