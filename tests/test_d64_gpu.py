@@ -68,6 +68,32 @@ def test_prologue_d64_edge_values(sage_lib):
         _prologue(qt, kt, vt, "NHD", smooth)
 
 
+def test_prologue_d64_key_sum_exponent_spread(sage_lib):
+    # Chunks whose key magnitudes in a channel span 20 to 50 binades: the
+    # float-pair chunk sums are taken where they are exact and the fp64 left-to-
+    # right sums elsewhere, per channel; ties of x/s and subnormal values mixed in.
+    rng = np.random.default_rng(640)
+    S, H = 1000, 2
+    q = rng.standard_normal((1, S, H, 64)).astype(np.float32)
+    k = rng.standard_normal((1, S, H, 64)).astype(np.float32)
+    v = rng.standard_normal((1, S, H, 64)).astype(np.float32)
+    for c in range(64):
+        spread = 20 + (c % 31)
+        for chunk in range(0, S, 32):
+            n = min(32, S - chunk)
+            sign = rng.choice([-1.0, 1.0], n)
+            vals = sign * np.ldexp(rng.uniform(1, 2, n), -spread)
+            big = rng.integers(0, n)
+            vals[big] = sign[big] * rng.uniform(1, 2) * 2.0 ** rng.integers(-2, 3)
+            k[0, chunk:chunk + n, c % H, c] = vals
+    v[0, 0:64, 1, 5] = np.round(rng.uniform(-448, 448, 64))   # many e4m3 ties once scaled
+    v[0, 3, 1, 5] = 448.0
+    dev = torch.device("cuda")
+    qt, kt, vt = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (q, k, v))
+    for smooth in (True, False):
+        _prologue(qt, kt, vt, "NHD", smooth)
+
+
 @pytest.mark.parametrize("s_len", [1, 127, 129, 300, 1000])
 @pytest.mark.parametrize("causal", [False, True])
 def test_attention_d64_matches_oracle(sage_lib, s_len, causal):
