@@ -23,9 +23,10 @@
 // rint_even(x*r) in its low byte; x*r and fl(x/s) are both within 2^-17 of
 // x/s (|x/s| <= 127.5), so when |fl(c - x*r)| < 1/2 - 2^-15 the code c is
 // rint_even(fl(x/s)); otherwise the division decides. e4m3: rounding is
-// monotone and fl(v/s) lies within 2^-22 relative of q = fl(v*fl(1/s)), so
-// when q*(1 - 2^-21) and q*(1 + 2^-21) round to the same code, that is the
-// code of fl(v/s); otherwise the division decides. Key sums: a TwoSum chain
+// monotone and fl(v/s) lies within 2^-22 relative of q = fl(v*r), r within
+// one ulp of 1/s, so when q*(1 - 2^-21) and q*(1 + 2^-21) round to the same
+// code, that is the code of fl(v/s); otherwise q decides if q*s == v
+// exactly (v/s sits on a code boundary), else the division. Key sums: a TwoSum chain
 // of float pairs over the chunk's 32 tokens is exact while the largest and
 // the smallest nonzero magnitude of a channel in the chunk are at most 2^36
 // apart (inputs are multiples of 2^L, partial sums stay below 2^(E+6), each
@@ -110,9 +111,26 @@ __device__ __noinline__ uint32_t exact_code_bits(float x, float s) {
   return __float_as_uint(__fadd_rn(__fdiv_rn(x, s), kMagic));
 }
 
+// 1/x to within one ulp (x normal): enough for the V codes' brackets.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The correctly rounded quotient v / s for the exact path of a V code: q =
+// fl(v*r) itself when q*s == v exactly, else the division (r = 0 marks a
+// scale the fast path does not take; |v| >= 2^-90 keeps a nonzero residual
+// v - q*s above the fp32 underflow threshold).
+__device__ __forceinline__ float v_quotient(float v, float s, float r) {
+  const float q = __fmul_rn(v, r);
+  if (r != 0.0f && fabsf(v) >= 0x1p-90f && __fmaf_rn(-q, s, v) == 0.0f) return q;
+  return __fdiv_rn(v, s);
+}
+
 // Exact path of a pair of e4m3 codes (low byte channel 2l): rare.
-__device__ __noinline__ uint32_t exact_v_pair(uint32_t w, float s0, float s1) {
-  return e4m3x2(__fdiv_rn(hi_bf16(w), s1), __fdiv_rn(lo_bf16(w), s0));
+__device__ __noinline__ uint32_t exact_v_pair(uint32_t w, float2 s, float2 r) {
+  return e4m3x2(v_quotient(hi_bf16(w), s.y, r.y), v_quotient(lo_bf16(w), s.x, r.x));
 }
 
 // INT8 codes of one 32-token block of this lane's two channels: x0 / x1 hold
@@ -356,7 +374,7 @@ __global__ void __launch_bounds__(kWarps * 32) p64_codes(const P64 p) {
   // V codes e4m3(fl(v / s_v)), transposed: 32 tokens of each of the lane's channels
   const float2 sv = *reinterpret_cast<const float2*>(p.out.v_scale + bh * kD + 2 * lane);
   const bool fast = (sv.x >= FLT_MIN || sv.x == 0.0f) && (sv.y >= FLT_MIN || sv.y == 0.0f);
-  const float2 rv = make_float2(sv.x >= FLT_MIN ? __frcp_rn(sv.x) : 0.0f, sv.y >= FLT_MIN ? __frcp_rn(sv.y) : 0.0f);
+  const float2 rv = make_float2(sv.x >= FLT_MIN ? rcp_approx(sv.x) : 0.0f, sv.y >= FLT_MIN ? rcp_approx(sv.y) : 0.0f);
   const uint32_t keep = (sv.x > 0.0f ? 0x00FFu : 0u) | (sv.y > 0.0f ? 0xFF00u : 0u);  // a zero channel has code 0
   const float2 dn = make_float2(kDn, kDn), up = make_float2(kUp, kUp);
   uint32_t pr[kChunkRows];  // low byte channel 2l, high byte channel 2l+1
@@ -375,7 +393,7 @@ __global__ void __launch_bounds__(kWarps * 32) p64_codes(const P64 p) {
     // rare: tokens whose fast codes are not certain
 #pragma unroll
     for (int t = 0; t < kChunkRows; ++t)
-      if ((redo >> t) & 1u) pr[t] = exact_v_pair(wv[t], sv.x, sv.y) & keep;
+      if ((redo >> t) & 1u) pr[t] = exact_v_pair(wv[t], sv, rv) & keep;
   }
   uint32_t w0[8], w1[8];  // channel 2l / 2l+1: tokens 4j .. 4j+3
 #pragma unroll

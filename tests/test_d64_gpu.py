@@ -88,6 +88,10 @@ def test_prologue_d64_key_sum_exponent_spread(sage_lib):
             k[0, chunk:chunk + n, c % H, c] = vals
     v[0, 0:64, 1, 5] = np.round(rng.uniform(-448, 448, 64))   # many e4m3 ties once scaled
     v[0, 3, 1, 5] = 448.0
+    # a channel on e4m3 rounding boundaries with a power-of-two scale (2^-3)
+    e, m = rng.integers(-6, 8, S), rng.integers(8, 16, S)
+    v[0, :, 0, 11] = rng.choice([-1.0, 1.0], S) * (2 * m + 1) * np.ldexp(1.0, e - 4) / 8
+    v[0, 7, 0, 11] = 56.0
     dev = torch.device("cuda")
     qt, kt, vt = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (q, k, v))
     for smooth in (True, False):

@@ -107,6 +107,34 @@ def test_key_sum_exponent_spread_both_kernels(sage_lib, s_len):
     _bundle_matches(qt, kt, vt, "NHD", True)
 
 
+def _e4m3_midpoints(rng, n, scale):
+    """n values v with v / scale exactly halfway between two e4m3 values
+    (below 448, so that the channel maximum 448 * scale sets the scale)."""
+    e = rng.integers(-6, 8, n)
+    m = rng.integers(8, 16, n)
+    sign = rng.choice([-1.0, 1.0], n)
+    return sign * (2 * m + 1) * np.ldexp(1.0, e - 4) * scale
+
+
+@pytest.mark.parametrize("s_len", [300, 1300])
+def test_v_code_ties_both_kernels(sage_lib, s_len):
+    """V channels whose scale is a power of two (max |v| = 448 * 2^k) filled
+    with values on e4m3 rounding boundaries: the fast brackets straddle every
+    one of them, and the exact quotient must round half to even."""
+    rng = np.random.default_rng(31 + s_len)
+    H = 2
+    q = rng.standard_normal((1, s_len, H, 128)).astype(np.float32)
+    k = rng.standard_normal((1, s_len, H, 128)).astype(np.float32)
+    v = rng.standard_normal((1, s_len, H, 128)).astype(np.float32)
+    for c, scale in ((3, 1.0), (40, 0.125), (77, 2.0 ** -20), (127, 64.0)):
+        col = _e4m3_midpoints(rng, s_len, scale)
+        col[s_len // 2] = 448.0 * scale
+        v[0, :, c % H, c] = col
+    dev = torch.device("cuda")
+    qt, kt, vt = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (q, k, v))
+    _bundle_matches(qt, kt, vt, "NHD", True)
+
+
 @pytest.mark.parametrize("s_len", [96, 256, 1000])
 def test_sageattn_short_matches_oracle(sage_lib, s_len):
     w = custom(2, 4, s_len, seed_index=3300 + s_len, k_offset_std=2.0)
