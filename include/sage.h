@@ -146,6 +146,12 @@ SAGE_API int sage_quantize_scratch_size(int64_t B, int64_t S, int64_t H, int64_t
 /* Workspace bytes sage_sageattn needs: one bundle plus the quantize scratch. */
 SAGE_API int sage_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes);
 
+/* Device workspace bytes sage_sageattn_host needs for n_groups head groups
+ * (0: the library's choice): device copies of q, k, v and out, and one
+ * bundle plus quantize scratch for each of two groups in flight.
+ * Errors: as sage_bundle_size; ARG for n_groups < 0. */
+SAGE_API int sage_host_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, int n_groups, size_t* bytes);
+
 /* ------------------------------------------------------------- operations -- */
 
 /* The quantization prologue ("prepare"): optional smooth_k key mean (fp64
@@ -277,6 +283,30 @@ SAGE_API int sage_sageattn_ex(const void* q_dev, const void* k_dev, const void* 
                               float sm_scale, int smooth_k, void* out_dev, const int64_t out_strides[4],
                               int out_dtype, float* lse_dev, void* workspace_dev, size_t workspace_bytes,
                               void* cuda_stream);
+
+/* sageattn on HOST buffers, end to end: q, k, v and out live in host memory
+ * (page-locked memory lets the copies run asynchronously; pageable memory
+ * works, with staged copies), each contiguous in tensor_layout ("NHD":
+ * (B, S, H, D); "HND": (B, H, S, D)) with the given shape (the four tensors
+ * have one shape; dtype SAGE_DTYPE_BF16 for all four; D = 128 or 64).
+ * The heads are cut into n_groups groups (0: the library's choice, at most
+ * 16, at least about 32 MB of inputs per group). On internal streams, the
+ * inputs of each group are copied to the device (2-D copies), the prologue
+ * and the attention kernel of group g run on one of two compute streams in
+ * turn, and group g's output is copied back as soon as it is done; so copies
+ * overlap the kernels of the neighbouring groups. Work starts after what
+ * cuda_stream already holds and cuda_stream waits for the last copy back:
+ * the call is asynchronous like the device entries; synchronize cuda_stream
+ * before reading out_host. Results equal sage_sageattn_ex's (no LSE) on
+ * the same tensors in device memory.
+ * workspace_dev: sage_host_workspace_size(B, S, H, D, n_groups) bytes of
+ * device memory, 256-byte aligned, not used by another call at the same time.
+ * Errors: DTYPE, NULLPTR, LAYOUT, HEAD_DIM, SHAPE, TOO_LARGE, ARG (sm_scale,
+ * n_groups < 0), ALIGN, WORKSPACE, ARCH, CUDA. */
+SAGE_API int sage_sageattn_host(const void* q_host, const void* k_host, const void* v_host,
+                                const int64_t shape[4], int dtype, const char* tensor_layout, int is_causal,
+                                float sm_scale, int smooth_k, void* out_host, int n_groups, void* workspace_dev,
+                                size_t workspace_bytes, void* cuda_stream);
 
 /* ---------------------------------------------------------- diagnostics -- */
 

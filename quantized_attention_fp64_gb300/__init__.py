@@ -12,11 +12,13 @@ from .api import (  # noqa: F401
     attention,
     attention_simt,
     device_error,
+    host_workspace_size,
     lse_smooth_k_term,
     quantize,
     quantize_scratch_size,
     release_workspace_cache,
     sageattn,
     sageattn_ex,
+    sageattn_host,
     workspace_size,
 )

@@ -51,6 +51,9 @@ _SIGNATURES = {
     "sage_sageattn_ex": (c_int, [c_vp, c_vp, c_vp, I64x4, I64x4, I64x4, I64x4, I64x4, I64x4, c_int, c_int, c_int,
                                  ctypes.c_char_p, c_int, ctypes.c_float, c_int, c_vp, I64x4, c_int, c_vp, c_vp,
                                  ctypes.c_size_t, c_vp]),
+    "sage_host_workspace_size": (c_int, [c_i64, c_i64, c_i64, c_i64, c_int, c_size_p]),
+    "sage_sageattn_host": (c_int, [c_vp, c_vp, c_vp, I64x4, c_int, ctypes.c_char_p, c_int, ctypes.c_float, c_int, c_vp,
+                                   c_int, c_vp, ctypes.c_size_t, c_vp]),
     "sage_device_error": (c_int, [c_vp, ctypes.POINTER(c_int)]),
     "sage_strerror": (ctypes.c_char_p, [c_int]),
 }

@@ -351,6 +351,52 @@ def sageattn_ex(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm
     return _sageattn_call(True, q, k, v, tensor_layout, is_causal, sm_scale, return_lse, smooth_k, out, workspace)
 
 
+def host_workspace_size(B: int, S: int, H: int, D: int = 128, n_groups: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.load().sage_host_workspace_size(B, S, H, D, n_groups, ctypes.byref(n)))
+    return n.value
+
+
+def sageattn_host(q, k, v, tensor_layout: str = "NHD", is_causal: bool = False, sm_scale=None,
+                  smooth_k: bool = True, out=None, workspace=None, n_groups: int = 0, device=None):
+    """sageattn on host (CPU) tensors through sage_sageattn_host: the head
+    groups' copies to and from the GPU overlap the kernels of the other
+    groups. q, k, v: contiguous BF16 CPU tensors (pinned memory lets the
+    copies run asynchronously). Returns out, a CPU tensor (pinned when q is),
+    written asynchronously: synchronize the current CUDA stream before
+    reading it. The work runs on ``device`` (default: the current CUDA device)."""
+    for t in (q, k, v):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("expected torch tensors")
+        if t.is_cuda:
+            raise ValueError("sageattn_host takes host (CPU) tensors; use sageattn for device tensors")
+        if not t.is_contiguous():
+            raise SageError(SAGE_ERR_LAYOUT, "host tensors must be contiguous")
+    if q.dim() != 4 or tuple(q.shape) != tuple(k.shape) or tuple(q.shape) != tuple(v.shape):
+        raise SageError(SAGE_ERR_SHAPE, "q, k and v must have identical 4-d shapes")
+    lib = _lib.load()
+    layout = tensor_layout if isinstance(tensor_layout, str) else str(tensor_layout)
+    B, S, H, D = _bsh(tuple(q.shape), layout)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=q.is_pinned())
+    elif out.is_cuda or not out.is_contiguous() or tuple(out.shape) != tuple(q.shape):
+        raise SageError(SAGE_ERR_SHAPE, "out must be a contiguous host tensor of q's shape")
+    with torch.cuda.device(dev):
+        n = ctypes.c_size_t(0)
+        rc = lib.sage_host_workspace_size(B, S, H, D, n_groups, ctypes.byref(n))
+        if rc == 0 and (workspace is None or workspace.numel() < n.value):
+            workspace = torch.empty(max(n.value, 256), dtype=torch.uint8, device=dev)
+        scale = float("nan") if sm_scale is None else float(sm_scale)
+        rc = lib.sage_sageattn_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), _i64x4(tuple(q.shape)), _dtype_code(q),
+                                    _LAYOUTS.get(layout) or layout.encode(), int(bool(is_causal)), scale,
+                                    int(bool(smooth_k)), out.data_ptr(), int(n_groups),
+                                    workspace.data_ptr() if workspace is not None else None,
+                                    workspace.numel() if workspace is not None else 0, _stream_handle(dev.index))
+    _check(rc)
+    return out
+
+
 def device_error(device=None) -> int:
     """Synchronizes the current stream and returns (and clears) the device error word."""
     lib = _lib.load()

@@ -256,6 +256,176 @@ int sageattn_impl(const void* q_dev, const void* k_dev, const void* v_dev, const
   return SAGE_OK;
 }
 
+// ------------------------------------------------------------ host buffers --
+// sage_sageattn_host: host-resident q, k, v and out. The heads are cut into
+// G groups; one internal stream copies the groups' inputs in (2-D copies: a
+// group is a column block of every token row in NHD, a block of heads of
+// every batch in HND), two compute streams take the groups in turn (the
+// prologue and attention of group g), one stream copies the outputs back. So
+// the copies of one group overlap the kernels of its neighbours, and one
+// group's attention tail overlaps the next group's kernels.
+
+constexpr int kHostMaxGroups = 16;
+constexpr size_t kHostGroupBytes = size_t(32) << 20;  // aim: at least 32 MB of inputs per group
+
+struct HostPlan {
+  int64_t hg = 0, G = 0;  // heads per group, groups
+  size_t grp_in = 0;      // bytes of one bf16 tensor of a group
+  size_t off_q = 0, off_k = 0, off_v = 0, off_o = 0, off_bundle[2] = {0, 0}, off_scratch[2] = {0, 0}, total = 0;
+};
+
+HostPlan host_plan(int64_t B, int64_t S, int64_t H, int64_t D, int n_groups) {
+  HostPlan p;
+  const size_t in_bytes = static_cast<size_t>(B * S * H * D) * 2;
+  int64_t G = n_groups;
+  if (G <= 0) {
+    // at most 10 groups unless asked: at the video size (28 heads) 10 groups
+    // of 3 heads measured 2.79 ms, 7 of 4 2.87, 14 of 2 3.08 per call
+    G = static_cast<int64_t>(3 * in_bytes / kHostGroupBytes);
+    G = G < 1 ? 1 : (G > 10 ? 10 : G);
+  }
+  if (G > kHostMaxGroups) G = kHostMaxGroups;
+  if (G > H) G = H > 0 ? H : 1;
+  p.hg = H > 0 ? div_up(H, G) : 1;
+  p.G = H > 0 ? div_up(H, p.hg) : 1;
+  p.grp_in = static_cast<size_t>(B * S * p.hg * D) * 2;
+  const size_t region = round256(p.grp_in * static_cast<size_t>(p.G));
+  const size_t bundle = bundle_layout(B, S, p.hg, D).total;
+  const size_t scratch = round256(prologue_scratch_bytes(B, S, p.hg, D));
+  size_t o = 0;
+  p.off_q = o;
+  o += region;
+  p.off_k = o;
+  o += region;
+  p.off_v = o;
+  o += region;
+  p.off_o = o;
+  o += region;
+  for (int i = 0; i < 2; ++i) {
+    p.off_bundle[i] = o;
+    o += bundle;
+    p.off_scratch[i] = o;
+    o += scratch;
+  }
+  p.total = o;
+  return p;
+}
+
+// Internal streams and events, created once per device; the enqueue of one
+// call holds the device's lock (the events are reused call after call).
+struct HostStreams {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp[2] = {nullptr, nullptr};
+  cudaEvent_t ev[2 + 2 * kHostMaxGroups] = {};
+};
+HostStreams g_host[kMaxDevices];
+std::mutex g_host_mu[kMaxDevices];
+
+cudaError_t host_streams(int dev, HostStreams** out) {
+  HostStreams& h = g_host[dev];
+  if (!h.ready) {
+    cudaError_t e;
+    cudaStream_t* ss[4] = {&h.h2d, &h.d2h, &h.comp[0], &h.comp[1]};
+    for (cudaStream_t* st : ss)
+      if (*st == nullptr && (e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    for (cudaEvent_t& ev : h.ev)
+      if (ev == nullptr && (e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+    h.ready = true;
+  }
+  *out = &h;
+  return cudaSuccess;
+}
+
+// The 2-D copy of heads [h0, h0 + n) of one bf16 tensor between its full
+// host layout and the group's packed device layout (either direction).
+cudaError_t copy_heads(void* dst, const void* src, bool to_device, bool nhd, int64_t B, int64_t S, int64_t H,
+                       int64_t D, int64_t h0, int64_t n, cudaStream_t st) {
+  const size_t e = 2;
+  const size_t row_full = static_cast<size_t>(nhd ? H * D : H * S * D) * e;  // pitch of the full tensor
+  const size_t row_grp = static_cast<size_t>(nhd ? n * D : n * S * D) * e;   // pitch of the group
+  const size_t col0 = static_cast<size_t>(nhd ? h0 * D : h0 * S * D) * e;    // first byte of the group in a row
+  const size_t rows = static_cast<size_t>(nhd ? B * S : B);
+  if (to_device)
+    return cudaMemcpy2DAsync(dst, row_grp, static_cast<const char*>(src) + col0, row_full, row_grp, rows,
+                             cudaMemcpyDefault, st);
+  return cudaMemcpy2DAsync(static_cast<char*>(dst) + col0, row_full, src, row_grp, row_grp, rows, cudaMemcpyDefault,
+                           st);
+}
+
+int sageattn_host_impl(const void* q_host, const void* k_host, const void* v_host, const int64_t shape[4],
+                       int dtype, const char* tensor_layout, bool causal, float sm_scale, int smooth_k,
+                       void* out_host, int n_groups, void* workspace_dev, size_t workspace_bytes,
+                       void* cuda_stream) {
+  if (dtype != SAGE_DTYPE_BF16) return SAGE_ERR_DTYPE;
+  if (shape == nullptr || tensor_layout == nullptr) return SAGE_ERR_NULLPTR;
+  bool nhd;
+  if (std::strcmp(tensor_layout, "NHD") == 0) nhd = true;
+  else if (std::strcmp(tensor_layout, "HND") == 0) nhd = false;
+  else return SAGE_ERR_LAYOUT;
+  const int64_t B = shape[0], S = nhd ? shape[1] : shape[2], H = nhd ? shape[2] : shape[1], D = shape[3];
+  int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  if (!(std::isnan(sm_scale) || (std::isfinite(sm_scale) && sm_scale > 0.0f))) return SAGE_ERR_ARG;
+  if (n_groups < 0) return SAGE_ERR_ARG;
+  const float scale = std::isnan(sm_scale) ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) : sm_scale;
+  if (B == 0 || H == 0 || S == 0) return SAGE_OK;
+  if (q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr || workspace_dev == nullptr)
+    return SAGE_ERR_NULLPTR;
+  if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return SAGE_ERR_ALIGN;
+  const HostPlan pl = host_plan(B, S, H, D, n_groups);
+  if (workspace_bytes < pl.total) return SAGE_ERR_WORKSPACE;
+  int dev = 0;
+  if ((rc = check_device(&dev)) != SAGE_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_host_mu[dev]);
+  HostStreams* hs = nullptr;
+  if (host_streams(dev, &hs) != cudaSuccess) return SAGE_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace_dev);
+  cudaStream_t user = static_cast<cudaStream_t>(cuda_stream);
+  cudaEvent_t ev_start = hs->ev[0], ev_end = hs->ev[1];
+  cudaEvent_t* ev_in = hs->ev + 2;
+  cudaEvent_t* ev_done = hs->ev + 2 + kHostMaxGroups;
+  cudaError_t e = cudaEventRecord(ev_start, user);
+  // every internal stream starts after the work already on the caller's stream
+  cudaStream_t all[4] = {hs->h2d, hs->d2h, hs->comp[0], hs->comp[1]};
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(all[i], ev_start, 0);
+  const void* src[3] = {q_host, k_host, v_host};
+  const size_t off_in[3] = {pl.off_q, pl.off_k, pl.off_v};
+  for (int64_t g = 0; g < pl.G && e == cudaSuccess; ++g) {
+    const int64_t h0 = g * pl.hg, n = (H - h0 < pl.hg) ? H - h0 : pl.hg;
+    for (int t = 0; t < 3 && e == cudaSuccess; ++t)
+      e = copy_heads(ws + off_in[t] + g * pl.grp_in, src[t], true, nhd, B, S, H, D, h0, n, hs->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in[g], hs->h2d);
+  }
+  for (int64_t g = 0; g < pl.G && e == cudaSuccess; ++g) {
+    const int64_t h0 = g * pl.hg, n = (H - h0 < pl.hg) ? H - h0 : pl.hg;
+    cudaStream_t c = hs->comp[g & 1];
+    if ((e = cudaStreamWaitEvent(c, ev_in[g], 0)) != cudaSuccess) break;
+    // the group's packed tensors: [B][S][n][D] (NHD) or [B][n][S][D] (HND)
+    const int64_t sb = S * n * D, ss = nhd ? n * D : D, sh = nhd ? D : S * D;
+    const Bf16In qi{reinterpret_cast<const uint16_t*>(ws + pl.off_q + g * pl.grp_in), sb, ss, sh};
+    const Bf16In ki{reinterpret_cast<const uint16_t*>(ws + pl.off_k + g * pl.grp_in), sb, ss, sh};
+    const Bf16In vi{reinterpret_cast<const uint16_t*>(ws + pl.off_v + g * pl.grp_in), sb, ss, sh};
+    const Out o{reinterpret_cast<uint16_t*>(ws + pl.off_o + g * pl.grp_in), sb, ss, sh};
+    const Bundle bundle = carve(ws + pl.off_bundle[g & 1], bundle_layout(B, S, n, D));
+    if ((e = launch_prologue(qi, ki, vi, B, S, n, D, smooth_k != 0, bundle, ws + pl.off_scratch[g & 1], false,
+                             g_err_ptr[dev], c)) != cudaSuccess)
+      break;
+    if ((e = launch_attention_tc(bundle, B, S, n, D, scale, o, causal, nullptr, g_err_ptr[dev], c)) != cudaSuccess)
+      break;
+    e = cudaEventRecord(ev_done[g], c);
+  }
+  for (int64_t g = 0; g < pl.G && e == cudaSuccess; ++g) {
+    const int64_t h0 = g * pl.hg, n = (H - h0 < pl.hg) ? H - h0 : pl.hg;
+    if ((e = cudaStreamWaitEvent(hs->d2h, ev_done[g], 0)) != cudaSuccess) break;
+    e = copy_heads(out_host, ws + pl.off_o + g * pl.grp_in, false, nhd, B, S, H, D, h0, n, hs->d2h);
+  }
+  // the caller's stream resumes once every output group is back (the last
+  // copy-out follows every kernel: each copy waited for its group)
+  if (e == cudaSuccess) e = cudaEventRecord(ev_end, hs->d2h);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(user, ev_end, 0);
+  return cuda_status(e);
+}
+
 }  // namespace
 }  // namespace sage
 
@@ -301,6 +471,22 @@ int sage_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* byte
   if (rc != SAGE_OK) return rc;
   *bytes = bundle_layout(B, S, H, D).total + prologue_scratch_bytes(B, S, H, D);
   return SAGE_OK;
+}
+
+int sage_host_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, int n_groups, size_t* bytes) {
+  if (bytes == nullptr) return SAGE_ERR_NULLPTR;
+  const int rc = check_sizes(B, S, H, D);
+  if (rc != SAGE_OK) return rc;
+  if (n_groups < 0) return SAGE_ERR_ARG;
+  *bytes = host_plan(B, S, H, D, n_groups).total;
+  return SAGE_OK;
+}
+
+int sage_sageattn_host(const void* q_host, const void* k_host, const void* v_host, const int64_t shape[4],
+                       int dtype, const char* tensor_layout, int is_causal, float sm_scale, int smooth_k,
+                       void* out_host, int n_groups, void* workspace_dev, size_t workspace_bytes, void* cuda_stream) {
+  return sageattn_host_impl(q_host, k_host, v_host, shape, dtype, tensor_layout, is_causal != 0, sm_scale, smooth_k,
+                            out_host, n_groups, workspace_dev, workspace_bytes, cuda_stream);
 }
 
 int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k, const sage_bf16_tensor* v, int64_t B,

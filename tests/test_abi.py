@@ -183,3 +183,43 @@ def test_sageattn_ex_keeps_the_other_checks(lib, over, code):
     # the extended entry honours is_causal and the log-sum-exp (here both on)
     # and still rejects everything else sage_sageattn rejects
     assert _call_sageattn_ex(lib, **over) == code
+
+
+def _call_sageattn_host(lib, **over):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, shape=(1, 256, 2, 128), dt=0, layout=b"NHD", causal=0,
+             sm=float("nan"), smooth=1, out=0x40000, groups=0, ws=0x50000, wsn=1 << 40)
+    a.update(over)
+    return lib.sage_sageattn_host(ctypes.c_void_p(a["q"]), ctypes.c_void_p(a["k"]), ctypes.c_void_p(a["v"]),
+                                  _lib.I64x4(*a["shape"]), a["dt"], a["layout"], a["causal"], ctypes.c_float(a["sm"]),
+                                  a["smooth"], ctypes.c_void_p(a["out"]), a["groups"], ctypes.c_void_p(a["ws"]),
+                                  a["wsn"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dt=1), DTYPE), (dict(layout=b"BSHD"), LAYOUT), (dict(layout=None), NULLPTR),
+    (dict(shape=(1, 256, 2, 96)), HEAD_DIM), (dict(shape=(1, -1, 2, 128)), SHAPE),
+    (dict(shape=(1, 1 << 32, 2, 128)), TOO_LARGE), (dict(sm=0.0), ARG), (dict(groups=-1), ARG),
+    (dict(q=0), NULLPTR), (dict(out=0), NULLPTR), (dict(ws=0), NULLPTR), (dict(ws=0x50010), ALIGN),
+    (dict(wsn=1000), WORKSPACE),
+])
+def test_sageattn_host_rejections(lib, over, code):
+    # every argument check runs on the host before any CUDA call
+    assert _call_sageattn_host(lib, **over) == code
+
+
+def test_sageattn_host_empty_problem_does_nothing(lib):
+    assert _call_sageattn_host(lib, shape=(1, 0, 2, 128), q=0, k=0, v=0, out=0, ws=0, wsn=0) == OK
+    assert _call_sageattn_host(lib, shape=(0, 256, 2, 128), layout=b"HND") == OK
+
+
+def test_host_workspace_size_grows_with_groups_in_flight(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.sage_host_workspace_size(1, 16384, 28, 128, 0, ctypes.byref(n)) == OK
+    auto = n.value
+    # device copies of q, k, v, out (4 x 117 MB) plus two groups' bundles and scratch
+    assert auto >= 4 * 16384 * 28 * 128 * 2
+    assert lib.sage_host_workspace_size(1, 16384, 28, 128, 1, ctypes.byref(n)) == OK
+    one = n.value  # one group of 28 heads: two full-size bundles
+    assert one > auto
+    assert lib.sage_host_workspace_size(1, 16384, 28, 128, -1, ctypes.byref(n)) == ARG
+    assert lib.sage_host_workspace_size(1, 16384, 28, 96, 0, ctypes.byref(n)) == HEAD_DIM
