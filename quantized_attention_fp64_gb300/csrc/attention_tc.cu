@@ -41,6 +41,13 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <memory>
+#include <mutex>
+#include <type_traits>
+#include <utility>
+#include <vector>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -104,11 +111,57 @@ struct Params {
   int* dev_err;
 };
 
+// Work-unit schedule of the causal kernel. With the mask, the unit of query
+// tiles (2p, 2p+1) of a head reads 2p + 2 key tiles, so round-robin units
+// leave CTAs unevenly loaded (82.6% of the busiest CTA's work on average at
+// B1 H28 S16384). The host assigns units heaviest first, within windows of a
+// few heads (their K and V stay in L2 together), each to the CTA with the
+// least work so far; CTA b takes units unit[start[b] .. start[b+1]) in that
+// order. n = 0: round robin (too many units or CTAs for the table).
+constexpr int kSchedMaxUnits = 7168;
+constexpr int kSchedMaxCtas = 160;
+struct Sched {
+  int32_t n;
+  uint16_t start[kSchedMaxCtas + 1];
+  uint16_t unit[kSchedMaxUnits];
+};
+struct NoSched {};
+template <bool kCausal>
+using SchedOf = typename std::conditional<kCausal, Sched, NoSched>::type;
+
 // Key tiles query tile `qt` reads: all of them, or with the causal mask the
 // tiles up to its diagonal (Q and K have the same length).
 template <bool kCausal>
 __device__ __forceinline__ int64_t key_tiles(const Params& prm, int64_t qt) {
   return kCausal ? min(prm.n_kv, qt + 1) : prm.n_kv;
+}
+
+// This CTA's units. Without a schedule: u = blockIdx.x, + grid, + 2 grid, ...
+// while u < n_units. With one: the table's entries, then -1.
+template <bool kCausal>
+__device__ __forceinline__ int64_t first_unit(const SchedOf<kCausal>& sc) {
+  if constexpr (kCausal) {
+    if (sc.n > 0) return sc.start[blockIdx.x] < sc.start[blockIdx.x + 1] ? sc.unit[sc.start[blockIdx.x]] : -1;
+  }
+  return blockIdx.x;
+}
+template <bool kCausal>
+__device__ __forceinline__ bool unit_valid(const Params& prm, const SchedOf<kCausal>& sc, int64_t u) {
+  if constexpr (kCausal) {
+    if (sc.n > 0) return u >= 0;
+  }
+  return u < prm.n_units;
+}
+// the unit after u, which is this CTA's k-th (k >= 1)
+template <bool kCausal>
+__device__ __forceinline__ int64_t next_unit(const SchedOf<kCausal>& sc, int64_t u, int64_t k) {
+  if constexpr (kCausal) {
+    if (sc.n > 0) {
+      const int64_t i = static_cast<int64_t>(sc.start[blockIdx.x]) + k;
+      return i < sc.start[blockIdx.x + 1] ? static_cast<int64_t>(sc.unit[i]) : -1;
+    }
+  }
+  return u + gridDim.x;
 }
 
 struct Ctx {
@@ -324,7 +377,8 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& cx, int i, uint32_t tS, 
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+                        const __grid_constant__ CUtensorMap tm_v, const Params prm,
+                        const __grid_constant__ SchedOf<kCausal> sched) {
   using L = Smem<D>;
   using T = SmemTail<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -388,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kKStages; ++s) k_pending[s] = -1;
         for (int s = 0; s < kVStages; ++s) v_pending[s] = -1;
         bool ok = true;
-        for (int64_t u = blockIdx.x; ok && u < prm.n_units; u += gridDim.x) {
+        for (int64_t uk = 1, u = first_unit<kCausal>(sched); ok && unit_valid<kCausal>(prm, sched, u);
+         u = next_unit<kCausal>(sched, u, uk++)) {
           const int32_t bh = static_cast<int32_t>(u / prm.pairs_per_head);
           const int32_t q_row0 = static_cast<int32_t>((u % prm.pairs_per_head) * 256);
           // both query tiles (two 64-channel boxes each)
@@ -449,7 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dp = tc::sw128_desc(sbase + L::kOffP + static_cast<uint32_t>(i) * kTile8);
       uint32_t k_cnt = 0, v_cnt = 0, u_cnt = 0, sf_cnt = 0, p_cnt = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < prm.n_units; u += gridDim.x) {
+      for (int64_t uk = 1, u = first_unit<kCausal>(sched); ok && unit_valid<kCausal>(prm, sched, u);
+         u = next_unit<kCausal>(sched, u, uk++)) {
         if (!(ok = wait_bar_warp(cx, cx.bar(kBarQFull), u_cnt & 1u))) break;
         // this tile's key tiles, and the unit's (the ring carries the larger
         // count; a tile releases the stages it does not use without an MMA)
@@ -524,7 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t nblk = prm.S_pad / kQKBlock;
     uint32_t s_cnt = 0, pv_cnt = 0, vs_cnt = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < prm.n_units; u += gridDim.x) {
+    for (int64_t uk = 1, u = first_unit<kCausal>(sched); ok && unit_valid<kCausal>(prm, sched, u);
+         u = next_unit<kCausal>(sched, u, uk++)) {
       const int64_t bh = u / prm.pairs_per_head;
       const int64_t qrow = (u % prm.pairs_per_head) * 256 + i * 128 + row;  // query index in the head
       const bool row_valid = qrow < prm.S;
@@ -655,6 +712,56 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void
   return make_tmap(m, dt, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The causal schedule for (units, pairs per head, key tiles, grid), built once
+// and kept (a handful of shapes). Null when the table cannot hold it.
+const Sched* causal_schedule(int64_t n_units, int64_t pairs, int64_t n_kv, int grid) {
+  if (n_units > kSchedMaxUnits || grid > kSchedMaxCtas || grid <= 0) return nullptr;
+  struct Entry {
+    int64_t n_units, pairs, n_kv;
+    int grid;
+    std::unique_ptr<Sched> sched;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.n_units == n_units && e.pairs == pairs && e.n_kv == n_kv && e.grid == grid) return e.sched.get();
+  constexpr int64_t kWindowHeads = 4;  // heads whose units are ordered together
+  constexpr int64_t kUnitOverhead = 2; // fixed cost of a unit, in key tiles
+  const int64_t heads = n_units / pairs;
+  std::vector<int64_t> order;
+  order.reserve(static_cast<size_t>(n_units));
+  for (int64_t h0 = 0; h0 < heads; h0 += kWindowHeads)
+    for (int64_t pp = pairs - 1; pp >= 0; --pp)
+      for (int64_t h = h0; h < std::min(heads, h0 + kWindowHeads); ++h) order.push_back(h * pairs + pp);
+  // longest processing time first: each unit to the least loaded CTA
+  std::vector<std::pair<int64_t, int>> heap;  // (-load, -cta): std heaps are max-heaps
+  for (int c = 0; c < grid; ++c) heap.emplace_back(0, -c);
+  std::make_heap(heap.begin(), heap.end());
+  std::vector<std::vector<uint16_t>> per(static_cast<size_t>(grid));
+  for (int64_t u : order) {
+    std::pop_heap(heap.begin(), heap.end());
+    auto top = heap.back();
+    heap.pop_back();
+    const int c = -top.second;
+    per[static_cast<size_t>(c)].push_back(static_cast<uint16_t>(u));
+    const int64_t tiles = std::min(n_kv, 2 * (u % pairs) + 2);
+    heap.emplace_back(top.first - (tiles + kUnitOverhead), top.second);
+    std::push_heap(heap.begin(), heap.end());
+  }
+  std::unique_ptr<Sched> sc(new Sched());
+  sc->n = static_cast<int32_t>(n_units);
+  int64_t pos = 0;
+  for (int c = 0; c < grid; ++c) {
+    sc->start[c] = static_cast<uint16_t>(pos);
+    for (uint16_t u : per[static_cast<size_t>(c)]) sc->unit[pos++] = u;
+  }
+  sc->start[grid] = static_cast<uint16_t>(pos);
+  if (cache.size() >= 16) cache.erase(cache.begin());
+  cache.push_back(Entry{n_units, pairs, n_kv, grid, std::move(sc)});
+  return cache.back().sched.get();
+}
+
 }  // namespace
 
 cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
@@ -685,11 +792,7 @@ cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t 
   p.sm_log2 = sm_scale * kLog2e;
   p.lse = lse;
   p.dev_err = dev_err;
-  auto kernel = D == 128 ? (causal ? attention_tc_kernel<128, true> : attention_tc_kernel<128, false>)
-                         : (causal ? attention_tc_kernel<64, true> : attention_tc_kernel<64, false>);
   const uint32_t smem_bytes = D == 128 ? SmemTail<128>::kBytes : SmemTail<64>::kBytes;
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kernel), static_cast<int>(smem_bytes));
-  if (e != cudaSuccess) return e;
   const int sms = sm_count_current();
   const int grid = static_cast<int>(p.n_units < sms ? p.n_units : sms);
   // programmatic dependent launch: the CTAs may start (barriers, TMEM,
@@ -705,7 +808,24 @@ cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+  cudaError_t e;
+  if (!causal) {
+    auto kernel = D == 128 ? attention_tc_kernel<128, false> : attention_tc_kernel<64, false>;
+    if ((e = set_smem_limit_once(reinterpret_cast<const void*>(kernel), static_cast<int>(smem_bytes))) !=
+        cudaSuccess)
+      return e;
+    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p, NoSched{});
+  }
+  auto kernel = D == 128 ? attention_tc_kernel<128, true> : attention_tc_kernel<64, true>;
+  if ((e = set_smem_limit_once(reinterpret_cast<const void*>(kernel), static_cast<int>(smem_bytes))) != cudaSuccess)
+    return e;
+  const Sched* sc = causal_schedule(p.n_units, p.pairs_per_head, p.n_kv, grid);
+  static const Sched round_robin = [] {
+    Sched r{};
+    r.n = 0;
+    return r;
+  }();
+  return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p, sc != nullptr ? *sc : round_robin);
 }
 
 }  // namespace sage
