@@ -70,37 +70,21 @@ def attention_peak(peaks):
 
 
 def dist_setup(n_gpus):
-    import torch
+    from quantized_attention_fp64_gb300 import dist
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    return rank, world, local
+    return dist.setup()
 
 
 def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
+    from quantized_attention_fp64_gb300 import dist
 
-        dist.barrier()
+    dist.barrier(world)
 
 
 def max_over_ranks(x, world):
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
+    from quantized_attention_fp64_gb300 import dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return dist.max_over_ranks(x, world)
 
 
 class ClockSampler:
@@ -482,10 +466,9 @@ def run_gpu(args):
         line["cpu_baseline"] = cpu_oracle_sample(rows=args.cpu_rows, heads=args.cpu_heads)
     if rank == 0:
         print(json.dumps(line))
-    if world > 1:
-        import torch.distributed as dist
+    from quantized_attention_fp64_gb300 import dist
 
-        dist.destroy_process_group()
+    dist.teardown(world)
     return 0
 
 
