@@ -100,7 +100,8 @@ constexpr float kLog2P = 8.807354922057604f;    // log2(448)
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct Params {
-  int64_t S, S_pad, n_kv, pairs_per_head, n_units;
+  int64_t S, S_pad, n_kv, pairs_per_head, n_units;  // pairs_per_head: units per head
+  int tiles;   // query tiles per unit: 2 (one per softmax warpgroup), or 1 when few units would leave SMs idle
   float* lse;  // [B][H][S] natural-log log-sum-exp of each row's logits, or null
   const float* q_scale;
   const float* k_scale;
@@ -393,14 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *cx.abort_flag = 0;
     tc::mbar_init(cx.bar(kBarQFull), 1);
-    tc::mbar_init(cx.bar(kBarQEmpty), 2);
+    // the MMA issuers of the unit's query tiles release Q, K and V stages
+    const uint32_t issuers = static_cast<uint32_t>(prm.tiles);
+    tc::mbar_init(cx.bar(kBarQEmpty), issuers);
     for (int s = 0; s < kKStages; ++s) {
       tc::mbar_init(cx.bar(kBarKFull + s), 1);
-      tc::mbar_init(cx.bar(kBarKEmpty + s), 2);
+      tc::mbar_init(cx.bar(kBarKEmpty + s), issuers);
     }
     for (int s = 0; s < kVStages; ++s) {
       tc::mbar_init(cx.bar(kBarVFull + s), 1);
-      tc::mbar_init(cx.bar(kBarVEmpty + s), 2);
+      tc::mbar_init(cx.bar(kBarVEmpty + s), issuers);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(cx.bar(kBarSFull + s), 1);
@@ -445,20 +448,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t uk = 1, u = first_unit<kCausal>(sched); ok && unit_valid<kCausal>(prm, sched, u);
          u = next_unit<kCausal>(sched, u, uk++)) {
           const int32_t bh = static_cast<int32_t>(u / prm.pairs_per_head);
-          const int32_t q_row0 = static_cast<int32_t>((u % prm.pairs_per_head) * 256);
-          // both query tiles (two 64-channel boxes each)
+          const int64_t qt0 = (u % prm.pairs_per_head) * prm.tiles;  // the unit's first query tile
+          const int32_t q_row0 = static_cast<int32_t>(qt0 * 128);
+          // the unit's query tiles (two 64-channel boxes each)
           if (!(ok = wait_bar(cx, cx.bar(kBarQEmpty), (u_cnt & 1u) ^ 1u))) break;
-          tc::mbar_arrive_expect_tx(cx.bar(kBarQFull), 2 * L::kTile16);
-#pragma unroll
-          for (int t = 0; t < 2; ++t)
+          tc::mbar_arrive_expect_tx(cx.bar(kBarQFull), static_cast<uint32_t>(prm.tiles) * L::kTile16);
+          for (int t = 0; t < prm.tiles; ++t)
 #pragma unroll
             for (int x = 0; x < D / 64; ++x)
               tc::tma_load_3d(sbase + L::kOffQ16 + t * L::kTile16 + x * kSub16, &tm_q, 64 * x, q_row0 + 128 * t, bh,
                               cx.bar(kBarQFull));
           q_pending = static_cast<int>(u_cnt & 1u);
           ++u_cnt;
-          // both query tiles' key tiles: those of the second, which sees more
-          const int64_t n_kv_u = key_tiles<kCausal>(prm, 2 * (u % prm.pairs_per_head) + 1);
+          // the unit's key tiles: those of its last query tile, which sees the most
+          const int64_t n_kv_u = key_tiles<kCausal>(prm, qt0 + prm.tiles - 1);
           for (int64_t j = 0; ok && j < n_kv_u; ++j) {
             const uint32_t ks = k_cnt % kKStages, kph = (k_cnt / kKStages) & 1u;
             if (!(ok = wait_bar(cx, cx.bar(kBarKEmpty + ks), kph ^ 1u))) break;
@@ -503,14 +506,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv0 = tc::sw128_desc(sbase + L::kOffV);
       const uint64_t dp = tc::sw128_desc(sbase + L::kOffP + static_cast<uint32_t>(i) * kTile8);
       uint32_t k_cnt = 0, v_cnt = 0, u_cnt = 0, sf_cnt = 0, p_cnt = 0;
-      bool ok = true;
+      bool ok = i < prm.tiles;  // with one query tile per unit the second issuer has no work
       for (int64_t uk = 1, u = first_unit<kCausal>(sched); ok && unit_valid<kCausal>(prm, sched, u);
          u = next_unit<kCausal>(sched, u, uk++)) {
         if (!(ok = wait_bar_warp(cx, cx.bar(kBarQFull), u_cnt & 1u))) break;
         // this tile's key tiles, and the unit's (the ring carries the larger
         // count; a tile releases the stages it does not use without an MMA)
-        const int64_t qt = 2 * (u % prm.pairs_per_head) + i;
-        const int64_t n_kv_i = key_tiles<kCausal>(prm, qt), n_kv_u = key_tiles<kCausal>(prm, qt | 1);
+        const int64_t qt0 = (u % prm.pairs_per_head) * prm.tiles, qt = qt0 + i;
+        const int64_t n_kv_i = key_tiles<kCausal>(prm, qt), n_kv_u = key_tiles<kCausal>(prm, qt0 + prm.tiles - 1);
         for (int64_t j = 0; ok && j <= n_kv_u; ++j) {
           if (j < n_kv_u) {
             // QK_j once K_j is loaded and the softmax has read S_{j-1}
@@ -579,11 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* p_row = smem + L::kOffP + static_cast<uint32_t>(i) * kTile8 + row * 128;
     const int64_t nblk = prm.S_pad / kQKBlock;
     uint32_t s_cnt = 0, pv_cnt = 0, vs_cnt = 0;
-    bool ok = true;
+    bool ok = i < prm.tiles;  // with one query tile per unit the second warpgroup has no work
     for (int64_t uk = 1, u = first_unit<kCausal>(sched); ok && unit_valid<kCausal>(prm, sched, u);
          u = next_unit<kCausal>(sched, u, uk++)) {
       const int64_t bh = u / prm.pairs_per_head;
-      const int64_t qrow = (u % prm.pairs_per_head) * 256 + i * 128 + row;  // query index in the head
+      const int64_t qt = (u % prm.pairs_per_head) * prm.tiles + i;  // this query tile
+      const int64_t qrow = qt * 128 + row;                             // query index in the head
       const bool row_valid = qrow < prm.S;
       const float cq = row_valid ? prm.q_scale[bh * nblk + qrow / kQKBlock] * prm.sm_log2 : 0.0f;
       const float* ks = prm.k_scale + bh * nblk;
@@ -598,7 +602,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K scales of a 128-key tile: 4 consecutive floats, 16-byte aligned
       // (S_pad / 32 is a multiple of 4)
       float4 ks_next = __ldg(reinterpret_cast<const float4*>(ks));
-      const int64_t qt = 2 * (u % prm.pairs_per_head) + i;  // this query tile
       const int64_t n_kv_i = key_tiles<kCausal>(prm, qt);
       for (int64_t j = 0; j < n_kv_i; ++j) {
         cb[0] = cq * ks_next.x;
@@ -782,7 +785,12 @@ cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t 
   p.S = S;
   p.S_pad = S_pad;
   p.n_kv = S_pad / kKeyTile;
-  p.pairs_per_head = div_up(S_pad / 128, 2);
+  const int sms = sm_count_current();
+  // one query tile per unit when that still fits the GPU in one wave (short
+  // sequences: twice the CTAs, each with half the chain); pairs otherwise,
+  // and always with the causal mask (its schedule is built on pairs)
+  p.tiles = (!causal && BH * (S_pad / 128) <= sms) ? 1 : 2;
+  p.pairs_per_head = div_up(S_pad / 128, p.tiles);
   p.n_units = BH * p.pairs_per_head;
   p.q_scale = in.q_scale;
   p.k_scale = in.k_scale;
@@ -793,7 +801,6 @@ cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t 
   p.lse = lse;
   p.dev_err = dev_err;
   const uint32_t smem_bytes = D == 128 ? SmemTail<128>::kBytes : SmemTail<64>::kBytes;
-  const int sms = sm_count_current();
   const int grid = static_cast<int>(p.n_units < sms ? p.n_units : sms);
   // programmatic dependent launch: the CTAs may start (barriers, TMEM,
   // tensor maps) while the previous kernel of the stream, normally the
