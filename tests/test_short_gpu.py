@@ -190,3 +190,27 @@ def test_back_to_back_calls_on_one_stream(sage_lib):
         torch.cuda.synchronize()
         assert torch.equal(o, alone)
     assert device_error() == 0
+
+
+def test_sageattn_short_reuses_one_workspace(sage_lib):
+    # calls that reuse one workspace (new inputs each time, and a torch
+    # kernel rewriting the inputs right before a call) must each see only
+    # their own prologue's output
+    ws = torch.empty(1 << 24, dtype=torch.uint8, device="cuda")
+    shapes = [(1, 4, 256), (2, 3, 700), (1, 4, 256), (1, 8, 1024)]
+    inputs = [make_qkv(custom(b, h, s, seed_index=3600 + i, k_offset_std=1.0), "cuda")
+              for i, (b, h, s) in enumerate(shapes)]
+    alone = []
+    for q, k, v in inputs:
+        alone.append(sageattn(q, k, v, sm_scale=SM))
+        torch.cuda.synchronize()
+    outs = [sageattn(q, k, v, sm_scale=SM, workspace=ws) for q, k, v in inputs]
+    q, k, v = inputs[0]
+    q2 = q.clone()
+    q2.mul_(-1.0)                                     # torch kernel right before the call
+    neg = sageattn(q2, k, v, sm_scale=SM, workspace=ws)
+    torch.cuda.synchronize()
+    for o, a in zip(outs, alone):
+        assert torch.equal(o, a)
+    assert torch.equal(neg, sageattn(-q, k, v, sm_scale=SM))
+    assert device_error() == 0
