@@ -32,6 +32,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = "B1_H28_S16384"
+METRIC = "attention TOPS at B1 H28 S16k D128 (frac of INT8/FP8 peak); prologue HBM GB/s"
+
+
+def bench_config(world=1):
+    """The workload named in both arms' JSON lines."""
+    return {"workload": WORKLOAD, "B": 1, "H": 28, "S": 16384, "D": 128, "smooth_k": True, "layout": "NHD",
+            "l2": "inputs (3 x 117 MB) larger than L2; no flush",
+            "parallelism": f"replicas x{world} (heads are independent)"}
 # DRAM traffic of one attention launch at this workload (dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture), valid only for the kernel source
 # it was taken on: reported when the source's SHA-256 prefix still matches.
@@ -198,12 +206,11 @@ def run_reference(args):
         base = b
     val = sum(t["value"] for t in times) / len(times)
     line = {
-        "impl": "reference", "metric": "attention TOPS at B1 H28 S16k D128", "value": val, "unit": "TOPS",
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TOPS",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * 4.0 * 28 * 16384 ** 2 * 128 / (val * 1e12), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8/e4m3 codes, fp32 softmax (numpy emulation)",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "B": 1, "H": 28, "S": 16384, "D": 128,
-                                        "smooth_k": True},
+        "data": "synthetic", "config": bench_config(args.gpus),
         "cpu_baseline": {k: base[k] for k in ("kind", "cores", "sample")} | {"value": val, "unit": "TOPS"},
         "e2e": {"value": val, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -419,7 +426,7 @@ def run_gpu(args):
     p_att, p16, p8 = attention_peak(peaks)
     att_tflops = ops / t_att / 1e12
     line = {
-        "metric": "attention TOPS at B1 H28 S16k D128 (frac of INT8/FP8 peak); prologue HBM GB/s",
+        "metric": METRIC,
         "value": world * ops / t_step / 1e12,
         "unit": "TOPS",
         "n_gpus": world,
@@ -431,9 +438,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "int8 QK (exact on fp16 tensor cores), e4m3 PV, fp32 softmax",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "S": S, "D": D, "smooth_k": True, "layout": "NHD",
-                   "l2": "inputs (3 x 117 MB) larger than L2; no flush",
-                   "parallelism": f"replicas x{world} (heads are independent)"},
+        "config": bench_config(world),
         "roofline": {"kernel": "attention_tc", "bound": "tensor", "achieved": att_tflops, "peak": p_att,
                      "unit": "TFLOP/s", "frac": att_tflops / p_att, "traffic": attention_traffic(),
                      "traffic_unit": "bytes per launch (DRAM read + write, one ncu capture)",
