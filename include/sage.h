@@ -139,7 +139,8 @@ SAGE_API int sage_bundle_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t
                      void* base_dev, sage_quantized* bundle);
 
 /* Scratch bytes sage_quantize needs (a work counter and per-head flags,
- * per-128-token partial key sums in fp64 and partial V maxima).
+ * per-128-token partial key sums in fp64 and partial V maxima, and each
+ * head's reciprocals of its V scales).
  * Errors: as sage_bundle_size. */
 SAGE_API int sage_quantize_scratch_size(int64_t B, int64_t S, int64_t H, int64_t D, size_t* bytes);
 
@@ -183,7 +184,7 @@ SAGE_API int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k,
  * that loads the library holds until the process exits. The web pages this
  * library follows have no counterpart to this entry point.
  * Limit: the problem must need at most 32 MiB of prologue scratch, i.e.
- * B * H * ceil(S / 128) * 128 * 12 bytes (each part rounded up to 256 bytes)
+ * B * H * (ceil(S / 128) * 128 * 12 + 512) bytes (each part rounded up to 256 bytes)
  * <= 32 MiB, about 21 800 (head, 128-token group) pairs; larger problems are
  * rejected with SAGE_ERR_WORKSPACE and nothing is launched.
  * The first call on each device looks up the array's device address with

@@ -81,7 +81,7 @@ constexpr int kFinCap = 32;  // heads waiting for their finish marker (see the p
 // needs (key mean and V scales, 1 KB); the barriers; per-stage item tags;
 // the event ring and the finish queue
 constexpr uint32_t kOffHstat = kStages * kTileBytes;
-constexpr uint32_t kHstatBytes = 2 * kHeadDim * 4;
+constexpr uint32_t kHstatBytes = 3 * kHeadDim * 4;  // key mean, V scales, their reciprocals
 constexpr uint32_t kOffBar = kOffHstat + kStages * kHstatBytes;
 constexpr int kNumBars = 2 * kStages + 2 * kEvents;  // full, empty, event full, event empty
 constexpr uint32_t kOffMeta = kOffBar + kNumBars * 8;
@@ -99,6 +99,7 @@ struct Params {
   unsigned* ready;  // [NH]: 1 once the head's key mean and V scales are written
   double* ksum;     // [NH][G][128]
   float* vmax;      // [NH][G][128]
+  float* vrcp;      // [NH][128]: fl(1/s_v) of each finished head (0 for s_v < FLT_MIN)
   int* dev_err;
 };
 
@@ -549,15 +550,14 @@ __device__ __forceinline__ void v_max_rows(const uint8_t* vr, int nv, int lane, 
 // vt_bh[(4*lane+c) * S_pad + s0]. Rows at or past nv get code 0. `release`
 // runs once the warp has stopped reading its rows.
 template <typename Release>
-__device__ __forceinline__ void v_codes_rows(const uint8_t* rows, int nv, int lane, float4 svs, uint8_t* vt_bh,
-                                             int64_t S_pad, int64_t s0, Release release) {
+__device__ __forceinline__ void v_codes_rows(const uint8_t* rows, int nv, int lane, float4 svs, float4 rvs,
+                                             uint8_t* vt_bh, int64_t S_pad, int64_t s0, Release release) {
   const float sc[4] = {svs.x, svs.y, svs.z, svs.w};
-  float rv[4];
+  const float rv[4] = {rvs.x, rvs.y, rvs.z, rvs.w};  // fl(1/s) for s >= FLT_MIN, else 0
   uint32_t keep = 0u;
   bool fast = true;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    rv[c] = sc[c] >= FLT_MIN ? __frcp_rn(sc[c]) : 0.0f;
     if (sc[c] > 0.0f) keep |= 0xFFu << (8 * c);
     fast = fast && (sc[c] >= FLT_MIN || sc[c] == 0.0f);  // zero channels are masked to code 0
   }
@@ -687,7 +687,9 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint32_t bar, uint32_t p
 
 // Finish head bh with the 256 threads of team 1: the pairwise tree over its
 // group key sums gives the key mean, the max over its group maxima the V
-// scales; then the head is published as ready. Every group of the head has
+// scales (and their correctly rounded reciprocals, which the codes items'
+// V codes multiply by, computed once here instead of once per item and warp);
+// then the head is published as ready. Every group of the head has
 // been counted (by the producer of this CTA, which saw the count complete).
 __device__ __forceinline__ void finish_head(const Params& prm, int64_t bh, int tt, double* fin_right,
                                             float* fin_vmax) {
@@ -713,7 +715,9 @@ __device__ __forceinline__ void finish_head(const Params& prm, int64_t bh, int t
       mu = __double2float_rn(__ddiv_rn(total, static_cast<double>(prm.S)));
     }
     prm.out.k_mean[bh * kHeadDim + c] = mu;
-    prm.out.v_scale[bh * kHeadDim + c] = __fdiv_rn(fmaxf(vmx, fin_vmax[c]), kE4M3Max);
+    const float vs = __fdiv_rn(fmaxf(vmx, fin_vmax[c]), kE4M3Max);
+    prm.out.v_scale[bh * kHeadDim + c] = vs;
+    prm.vrcp[bh * kHeadDim + c] = vs >= FLT_MIN ? __frcp_rn(vs) : 0.0f;
   }
   team_bar(1);
   if (tt == 0) {
@@ -936,6 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t hs = sbase + kOffHstat + st * kHstatBytes;
             tc::bulk_load(hs, prm.out.k_mean + it.bh * kHeadDim, kHeadDim * 4, cx.full(st));
             tc::bulk_load(hs + kHeadDim * 4, prm.out.v_scale + it.bh * kHeadDim, kHeadDim * 4, cx.full(st));
+            tc::bulk_load(hs + 2 * kHeadDim * 4, prm.vrcp + it.bh * kHeadDim, kHeadDim * 4, cx.full(st));
           }
           pending[st] = static_cast<int>(ph);
           ++cnt;
@@ -1073,11 +1078,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // codes item, team 0: V codes of this warp's 16 tokens, transposed to
       // [channel][token] (4-channel lanes); the V scales come with the K tile
       const float4 svs = *reinterpret_cast<const float4*>(hstat + st * (kHstatBytes / 4) + kHeadDim + 4 * lane);
+      const float4 rvs =
+          *reinterpret_cast<const float4*>(hstat + st * (kHstatBytes / 4) + 2 * kHeadDim + 4 * lane);
       tc::mbar_arrive(cx.empty(st));  // the K tile is team 1's
       const uint32_t c2 = cnt + 1;
       if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
       const uint32_t v_stage = c2 % kStages;
-      v_codes_rows(stage_rows(c2), nv, lane, svs, prm.out.vt_codes + bh * kHeadDim * S_pad, S_pad, s0,
+      v_codes_rows(stage_rows(c2), nv, lane, svs, rvs, prm.out.vt_codes + bh * kHeadDim * S_pad, S_pad, s0,
                    [&]() { tc::mbar_arrive(cx.empty(v_stage)); });
     } else {
       // codes item, team 1: K codes of k - mean; the key mean comes with the
@@ -1143,6 +1150,7 @@ __global__ void __launch_bounds__(kShortThreads, 1)
   __shared__ uint32_t g_max[kShortMaxGroups][kHeadDim];  // every group's max |v| bits
   __shared__ __align__(16) float h_mean[kHeadDim];
   __shared__ __align__(16) float h_vscale[kHeadDim];
+  __shared__ __align__(16) float h_vrcp[kHeadDim];
   __shared__ __align__(8) uint64_t bars[3];      // Q, K, V tile full
   __shared__ int abort_flag;
 
@@ -1228,7 +1236,8 @@ __global__ void __launch_bounds__(kShortThreads, 1)
     asm volatile("bar.sync 2, %0;" ::"n"(kShortThreads) : "memory");  // the V scales are in h_vscale
     // V codes, transposed (4-channel lanes)
     v_codes_rows(v_rows, nv, lane, *reinterpret_cast<const float4*>(h_vscale + 4 * lane),
-                 prm.out.vt_codes + bh * kHeadDim * S_pad, S_pad, s0, [] {});
+                 *reinterpret_cast<const float4*>(h_vrcp + 4 * lane), prm.out.vt_codes + bh * kHeadDim * S_pad,
+                 S_pad, s0, [] {});
   } else {
     // the group's exact key sums
     ok = wait_bar(cx, cx.full(1), 0);
@@ -1280,6 +1289,7 @@ __global__ void __launch_bounds__(kShortThreads, 1)
       const float vs = __fdiv_rn(vmx, kE4M3Max);
       h_mean[c] = mu;
       h_vscale[c] = vs;
+      h_vrcp[c] = vs >= FLT_MIN ? __frcp_rn(vs) : 0.0f;
       if (g == 0) {
         prm.out.k_mean[bh * kHeadDim + c] = mu;
         prm.out.v_scale[bh * kHeadDim + c] = vs;
@@ -1319,7 +1329,7 @@ __global__ void __launch_bounds__(kShortThreads, 1)
 }
 
 struct ScratchLayout {
-  size_t done_off, ready_off, ksum_off, vmax_off, header, total;
+  size_t done_off, ready_off, ksum_off, vmax_off, vrcp_off, header, total;
 };
 
 ScratchLayout scratch_layout(int64_t B, int64_t S, int64_t H) {
@@ -1333,7 +1343,8 @@ ScratchLayout scratch_layout(int64_t B, int64_t S, int64_t H) {
   l.header = l.ready_off + r256(NH * 4);
   l.ksum_off = l.header;
   l.vmax_off = l.ksum_off + r256(n * sizeof(double));
-  l.total = l.vmax_off + r256(n * sizeof(float));
+  l.vrcp_off = l.vmax_off + r256(n * sizeof(float));
+  l.total = l.vrcp_off + r256(NH * kHeadDim * sizeof(float));
   return l;
 }
 
@@ -1387,6 +1398,7 @@ cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, i
   p.ready = reinterpret_cast<unsigned*>(sc + l.ready_off);
   p.ksum = reinterpret_cast<double*>(sc + l.ksum_off);
   p.vmax = reinterpret_cast<float*>(sc + l.vmax_off);
+  p.vrcp = reinterpret_cast<float*>(sc + l.vrcp_off);
   p.dev_err = dev_err;
   CUtensorMap tq, tk, tv;
   const int aq = make_input_map(&tq, q, B, S, H), ak = make_input_map(&tk, k, B, S, H),

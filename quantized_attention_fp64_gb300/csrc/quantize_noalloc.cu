@@ -103,7 +103,7 @@ extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_
     if (!aligned16(p)) return SAGE_ERR_ALIGN;
   }
   // the built-in buffer bounds the problem size: B * H * ceil(S / 128) groups
-  // of 128 channels, 12 bytes each (plus alignment)
+  // of 128 channels, 12 bytes each, and 512 bytes per head (plus alignment)
   if (prologue_scratch_bytes(B, S, H, D) > kNoAllocScratch) return SAGE_ERR_WORKSPACE;
   void* scratch = noalloc_scratch_ptr(&rc);
   if (scratch == nullptr) return rc;

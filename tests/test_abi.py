@@ -54,8 +54,9 @@ def test_size_queries(lib):
     assert n.value >= 7 * B * H * S * 128   # int8/e4m3 codes (3) + fp16 Q/K copies (4)
     assert ws == n.value + sc
     # scratch: a 256-byte work counter, two per-head flag arrays (256-aligned),
-    # then fp64 + fp32 per (head, 128-token group, channel)
-    assert sc == 256 + 2 * 256 + 28 * 128 * 128 * 8 + 28 * 128 * 128 * 4
+    # then fp64 + fp32 per (head, 128-token group, channel), then the fp32
+    # reciprocals of each head's 128 V scales
+    assert sc == 256 + 2 * 256 + 28 * 128 * 128 * 8 + 28 * 128 * 128 * 4 + 28 * 128 * 4
     assert _sizes(lib, "sage_workspace_size", 1, 100, 2, 96)[0] == HEAD_DIM
     assert _sizes(lib, "sage_workspace_size", 1, 100, 2, 64)[0] == OK
     assert _sizes(lib, "sage_workspace_size", -1, 100, 2, 128)[0] == SHAPE
