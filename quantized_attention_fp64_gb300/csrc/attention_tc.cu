@@ -17,8 +17,11 @@
 //
 // Schedule (one persistent CTA per SM, 384 threads):
 //   warp 0      TMA producer: fp16 Q tiles, a 2-stage ring of fp16 K tiles
-//               (two 64-channel boxes per tile) and a 3-stage ring of e4m3
-//               V^T tiles, all in 128-byte-swizzled boxes.
+//               (two 64-channel boxes per tile) and a 4-stage ring of e4m3
+//               V^T tiles, all in 128-byte-swizzled boxes. A V tile is held
+//               until its PV completes, long after its K tile's QK, so the V
+//               ring is the deeper one: the producer, which loads K_j and
+//               V_j in turn, then rarely waits for a V stage.
 //   warp 1, 2   TMEM allocation (warp 1) and one MMA-issuing thread per query
 //               tile: each waits only on its own tile's events.
 //   warp 3      idle.
@@ -56,7 +59,7 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kKStages = 2;
-constexpr int kVStages = 3;
+constexpr int kVStages = 4;
 constexpr uint32_t kTile8 = 128 * 128;       // bytes of one e4m3 P tile (128 rows x 128 keys)
 constexpr uint32_t kSub16 = 128 * 128;       // bytes of one 64-channel fp16 subtile (128 rows)
 
@@ -84,9 +87,10 @@ template <int D>
 struct SmemTail {
   static constexpr uint32_t kOffTmemSlot = Smem<D>::kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffAbort = kOffTmemSlot + 8;
-  static constexpr uint32_t kOffVs = (kOffAbort + 8 + 15) / 16 * 16;  // [warpgroup][unit parity][D] fp32
-  static constexpr uint32_t kBytes = kOffVs + 4 * D * 4 + 1024;      // + alignment slack
+  static constexpr uint32_t kOffVs = (kOffAbort + 8 + 15) / 16 * 16;  // [warpgroup][D] fp32
+  static constexpr uint32_t kBytes = kOffVs + 2 * D * 4 + 1024;      // + alignment slack
 };
+static_assert(SmemTail<128>::kBytes <= 232448u, "shared memory of one CTA: at most 227 KB");
 
 // TMEM columns: S of query tile i at 128*i, O of query tile i (D columns) at 256 + D*i
 __host__ __device__ constexpr uint32_t col_s(int i) { return 128u * static_cast<uint32_t>(i); }
@@ -592,10 +596,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float cq = row_valid ? prm.q_scale[bh * nblk + qrow / kQKBlock] * prm.sm_log2 : 0.0f;
       const float* ks = prm.k_scale + bh * nblk;
       // the V scale of channel `row` (the first D threads) is copied into
-      // shared memory now, asynchronously, for the epilogue (double-buffered
-      // by unit: every thread of the warpgroup has finished the epilogue
-      // two units back before this thread passes the previous unit's wait)
-      float* vs_buf = reinterpret_cast<float*>(smem + T::kOffVs) + (2 * i + (vs_cnt & 1u)) * D;
+      // shared memory now, asynchronously, for the epilogue; the previous
+      // unit's epilogue has finished reading the buffer in every thread of
+      // the warpgroup once the O-empty barrier of that unit completes (all
+      // 128 threads arrive on it after their last read)
+      float* vs_buf = reinterpret_cast<float*>(smem + T::kOffVs) + i * D;
+      if (vs_cnt > 0 && !(ok = wait_bar_warp(cx, cx.bar(kBarOEmpty + i), (vs_cnt - 1) & 1u))) break;
       if (row < D) tc::cp_async4(tc::smem_u32(vs_buf + row), prm.v_scale + bh * D + row);
       float m = -INFINITY, l = 0.0f;
       float cb[4];
