@@ -84,7 +84,8 @@ enum {
   SAGE_ERR_CUDA = -11,          /* a CUDA runtime call or kernel launch failed */
   SAGE_ERR_DEVICE_TIMEOUT = -12,/* a kernel gave up waiting on an internal barrier (see sage_device_error) */
   SAGE_ERR_ARG = -13,           /* another invalid argument (e.g. non-finite or non-positive sm_scale) */
-  SAGE_ERR_TOO_LARGE = -14      /* sizes exceed the library's index limits */
+  SAGE_ERR_TOO_LARGE = -14,     /* sizes exceed the library's index limits */
+  SAGE_ERR_DEVICE_SMEM = -15    /* a kernel's dynamic shared memory was not 1024-byte aligned; it did no work */
 };
 
 /* dtype codes for sage_sageattn */
@@ -313,8 +314,11 @@ SAGE_API int sage_sageattn_host(const void* q_host, const void* k_host, const vo
 
 /* Synchronizes cuda_stream, then reads and clears the current device's error
  * word. Kernels set it (and return early) when a bounded wait on an internal
- * barrier runs out; they never trap. *code receives SAGE_OK or
- * SAGE_ERR_DEVICE_TIMEOUT. Returns SAGE_OK, NULLPTR or CUDA. */
+ * barrier runs out, or, before any work, when their dynamic shared memory is
+ * not 1024-byte aligned (the attention kernel uses all of it for aligned
+ * operand tiles); they never trap. *code receives SAGE_OK,
+ * SAGE_ERR_DEVICE_TIMEOUT or SAGE_ERR_DEVICE_SMEM. Returns SAGE_OK, NULLPTR
+ * or CUDA. */
 SAGE_API int sage_device_error(void* cuda_stream, int* code);
 
 /* Static description of an error code; never NULL. */

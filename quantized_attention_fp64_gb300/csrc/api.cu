@@ -586,7 +586,7 @@ int sage_device_error(void* cuda_stream, int* code) {
   if (cudaMemcpy(&v, g_err_ptr[dev], sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SAGE_ERR_CUDA;
   const int zero = 0;
   if (cudaMemcpy(g_err_ptr[dev], &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SAGE_ERR_CUDA;
-  *code = v == 0 ? SAGE_OK : SAGE_ERR_DEVICE_TIMEOUT;
+  *code = v == 0 ? SAGE_OK : (v == kDevErrSmemAlign ? SAGE_ERR_DEVICE_SMEM : SAGE_ERR_DEVICE_TIMEOUT);
   return SAGE_OK;
 }
 
@@ -607,6 +607,7 @@ const char* sage_strerror(int code) {
     case SAGE_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on an internal barrier";
     case SAGE_ERR_ARG: return "invalid argument (sm_scale must be finite and positive)";
     case SAGE_ERR_TOO_LARGE: return "sizes exceed the library's limits";
+    case SAGE_ERR_DEVICE_SMEM: return "a kernel found its shared memory window misaligned and did no work";
     default: return "unknown error code";
   }
 }

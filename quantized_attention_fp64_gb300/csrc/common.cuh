@@ -18,8 +18,10 @@ constexpr float kPScale = 448.0f;   // p in [0,1] is stored as e4m3(448 p)
 __host__ __device__ inline int64_t padded_len(int64_t s) { return (s + kKeyTile - 1) / kKeyTile * kKeyTile; }
 __host__ __device__ inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Device error word values (written by kernels that give up a bounded wait).
+// Device error word values: a kernel gave up a bounded wait, or found its
+// dynamic shared memory not 1024-byte aligned (it returns before any work).
 constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrSmemAlign = 2;
 
 // One BF16 input: element (b, s, h, d) at p[b*sb + s*ss + h*sh + d].
 struct Bf16In {

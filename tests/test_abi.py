@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_strerror_covers_codes(lib):
-    for code in range(0, -15, -1):
+    for code in range(0, -16, -1):
         msg = lib.sage_strerror(code)
         assert msg and b"unknown" not in msg
     assert b"unknown" in lib.sage_strerror(-99)

@@ -35,9 +35,18 @@ def test_tc_matches_oracle(sage_lib, w):
     _tc_vs_oracle(w)
 
 
-@pytest.mark.parametrize("s_len", [1, 33, 127, 129, 200, 1000, 4097])
+@pytest.mark.parametrize("s_len", [1, 33, 127, 129, 200, 1000, 2047, 2048, 2200, 4097])
 def test_tc_ragged_lengths(sage_lib, s_len):
+    # from 16 key tiles (S > 1920) the kernel runs with its correction
+    # warpgroup; below, the softmax warps rescale O themselves
     _tc_vs_oracle(custom(1, 2, s_len, seed_index=500 + s_len, k_offset_std=2.0))
+
+
+@pytest.mark.parametrize("B,H,S", [(2, 40, 2200), (1, 20, 3001)])
+def test_tc_tile_pairs_with_correction_warpgroup(sage_lib, B, H, S):
+    # enough heads for two query tiles per unit, long enough rows for the
+    # correction warpgroup, a ragged last key tile; sampled heads
+    _tc_vs_oracle(custom(B, H, S, seed_index=510 + H, k_offset_std=1.5), heads=[(0, 0), (B - 1, H - 1), (0, H // 2)])
 
 
 def test_tc_hnd_layout(sage_lib):
