@@ -74,7 +74,8 @@ static_assert(kChunks * 2 == kWarps, "two warps per 32-token chunk");
 
 // ring entries: a tile of one tensor, a marker to finish a head, the end
 enum : int { kTensorQ = 0, kTensorK = 1, kTensorV = 2, kFinish = 3, kEnd = 4 };
-constexpr int kEvents = 8;   // ring of "group done" events from team 1 to the producer
+constexpr int kEvents = 8;   // ring of "group done" events from the teams to the counter warp
+static_assert(kEvents % 2 == 0, "a report slot is always written by the same team");
 constexpr int kFinCap = 32;  // heads waiting for their finish marker (see the producer)
 
 // shared memory: kStages tiles; per stage the head statistics a codes item
@@ -733,10 +734,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const Params prm, int3 s_axis) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ double ks[kChunks][kHeadDim];            // exact chunk sums of the current group
-  __shared__ uint32_t vm[kWarps][kHeadDim / 2];       // per-warp max |v| bits, channel pairs
-  __shared__ float xk_hi[kChunks][kHeadDim], xk_lo[kChunks][kHeadDim];  // second-half key sums
-  __shared__ uint32_t xk_bits[kChunks][2];            // second-half magnitude bounds
+  // the statistics of the group a team is working on (either team can be)
+  __shared__ double ks[kTeams][kChunks][kHeadDim];            // exact chunk sums
+  __shared__ uint32_t vm[kTeams][kWarps][kHeadDim / 2];       // per-warp max |v| bits, channel pairs
+  __shared__ float xk_hi[kTeams][kChunks][kHeadDim], xk_lo[kTeams][kChunks][kHeadDim];  // second-half key sums
+  __shared__ uint32_t xk_bits[kTeams][kChunks][2];            // second-half magnitude bounds
   __shared__ float xa[2][kTeams * kWarps / 2][2];     // amax of each half block, two parities
   __shared__ float fin_vmax[kHeadDim];
   __shared__ double fin_right[kHeadDim];
@@ -776,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kTeams * kWarps + 1) {
     // --------------------------------------------------------------- counter --
-    // Counts the groups team 1 reports done. The fence and atomic of the count
+    // Counts the groups the teams report done. The fence and atomic of the count
     // stay off the compute warps and off the producer (a fence there would
     // also wait for its tile loads). When a head's last group is counted the
     // head goes into the finish queue; the producer turns it into a finish
@@ -790,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(cx.evt_empty(e));
         ++ev;
         if (h < 0) break;
-        // team 1's slot writes are ordered before the report (barrier, then
+        // the reporting team's slot writes are ordered before the report (barrier, then
         // release on the mbarrier); the fence makes them visible to the GPU
         // before the count
         __threadfence();
@@ -960,9 +962,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // --------------------------------------------------------------- compute --
   // Two teams of 8 warps work on different tiles of the same item. Stats
-  // item: team 0 the Q tile; team 1 the K sums, the V maxima and the group's
-  // results. Codes item: team 1 the K tile, team 0 the V tile. Warps 2c and
-  // 2c+1 of a team take the two halves (16 tokens each) of chunk c. Both
+  // item: role 0 the Q tile; role 1 the K sums, the V maxima and the group's
+  // results. Codes item: role 1 the K tile, role 0 the V tile. The teams swap
+  // roles from one item of a kind to the next (the two roles' work differs by
+  // about a quarter, and a team can run ahead of the other only as far as the
+  // ring allows; measured 4% faster than fixed roles at B1 H28 S16384).
+  // Finish markers always go to team 1. Warps 2c and 2c+1 of a team take the
+  // two halves (16 tokens each) of chunk c. Both
   // teams wait on every stage in ring order, so a parity wait never meets a
   // barrier two phases behind; a team releases the stages it does not use as
   // soon as they are full, and a stage is refilled once both have released it.
@@ -971,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t S = prm.S, S_pad = prm.S_pad, G = prm.G;
   const int64_t nblk = S_pad / kQKBlock;
   const uint32_t row_off = static_cast<uint32_t>(tw * kHalfRows * 256);
-  uint32_t cnt = 0, ev_cnt = 0;
+  uint32_t cnt = 0, n_stats = 0, n_codes = 0;  // ring position; items of each kind seen
   int xpar = 0;  // slot parity of the amax exchange (both warps of a pair flip together)
   // wait for ring position c to be full, then release it unused
   auto pass = [&](uint32_t c) -> bool {
@@ -988,8 +994,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tensor == kEnd) {
       if (team == 1 && tt == 0) {
         // tell the counter warp that no report follows
-        const uint32_t e = ev_cnt % kEvents;
-        if (wait_bar(cx, cx.evt_empty(e), ((ev_cnt / kEvents) & 1u) ^ 1u)) {
+        const uint32_t e = n_stats % kEvents;
+        if (wait_bar(cx, cx.evt_empty(e), ((n_stats / kEvents) & 1u) ^ 1u)) {
           evt_bh[e] = -1;
           tc::mbar_arrive(cx.evt_full(e));
         }
@@ -1004,6 +1010,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const Item it = decode_item(item, prm.NH, G, prm.lag);
     const uint32_t n_stages = it.phase == 0 ? (prm.smooth_k ? 3u : 2u) : 2u;
+    // the two teams swap roles from one item of a kind to the next, so that
+    // neither waits for the other's heavier tile (role 0: the Q tile of a
+    // stats item, the V tile of a codes item; role 1: the K and V tiles of a
+    // stats item, the K tile of a codes item)
+    const uint32_t kind_idx = it.phase == 0 ? n_stats++ : n_codes++;
+    const int role = team ^ static_cast<int>(kind_idx & 1u);
     const int64_t bh = it.bh;
     const int64_t s0c = it.g * kItemTokens + chunk * kQKBlock;  // first token of the chunk
     const int64_t s0 = s0c + sub * kHalfRows;                    // first token of this warp
@@ -1012,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile float* xo = &xa[xpar][pair][sub ^ 1];
     bool ok = true;
 
-    if (it.phase == 0 && team == 0) {
+    if (it.phase == 0 && role == 0) {
       // Q codes and scale
       const float2 nz[4] = {};
       int8_t* qc = prm.write_int8 ? prm.out.q_codes + bh * S_pad * kHeadDim : nullptr;
@@ -1034,8 +1046,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K tile: exact fp64 chunk sums, the second half's partial sums
         // joined into the first half's
         const uint32_t ks_stage = c2 % kStages;
-        key_chunk_sums(stage_rows(c2), nv, valid_rows(S, s0c, kQKBlock), sub, lane, pair, xk_hi[chunk],
-                       xk_lo[chunk], xk_bits[chunk], ks[chunk], [&]() { tc::mbar_arrive(cx.empty(ks_stage)); });
+        key_chunk_sums(stage_rows(c2), nv, valid_rows(S, s0c, kQKBlock), sub, lane, pair, xk_hi[team][chunk],
+                       xk_lo[team][chunk], xk_bits[team][chunk], ks[team][chunk],
+                       [&]() { tc::mbar_arrive(cx.empty(ks_stage)); });
         ++c2;
         if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
       }
@@ -1047,34 +1060,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 4; ++k) m4[k] = __vmaxu2(m4[k], __shfl_xor_sync(0xffffffffu, m4[k], 16));
       if (lane < 16) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) vm[tw][4 * lane + k] = m4[k];
+        for (int k = 0; k < 4; ++k) vm[team][tw][4 * lane + k] = m4[k];
       }
-      team_bar(1);
+      team_bar(team);
       if (tt < kHeadDim) {
         // the group's results: levels 1 and 2 of the pairwise tree over its 4
         // chunk sums, and its max |v| per channel
         const int c = tt;
         const int64_t slot = (bh * G + it.g) * kHeadDim + c;
-        if (prm.smooth_k) prm.ksum[slot] = __dadd_rn(__dadd_rn(ks[0][c], ks[1][c]), __dadd_rn(ks[2][c], ks[3][c]));
+        if (prm.smooth_k)
+          prm.ksum[slot] =
+              __dadd_rn(__dadd_rn(ks[team][0][c], ks[team][1][c]), __dadd_rn(ks[team][2][c], ks[team][3][c]));
         uint32_t mb = 0u;
 #pragma unroll
         for (int i = 0; i < kWarps; ++i) {
-          const uint32_t pr = vm[i][c >> 1];
+          const uint32_t pr = vm[team][i][c >> 1];
           mb = max(mb, (c & 1) ? (pr >> 16) : (pr & 0xFFFFu));
         }
         prm.vmax[slot] = __uint_as_float(mb << 16);
       }
-      team_bar(1);
+      team_bar(team);
       if (tt == 0) {
-        // report the group to the counter warp
-        const uint32_t e = ev_cnt % kEvents;
-        if (wait_bar(cx, cx.evt_empty(e), ((ev_cnt / kEvents) & 1u) ^ 1u)) {
+        // report the group to the counter warp; the report of the k-th
+        // stats item goes into slot k % kEvents, so each slot has one writer
+        // (kEvents is even and the roles alternate) and the counter warp
+        // reads the reports in ring order
+        const uint32_t e = kind_idx % kEvents;
+        if (wait_bar(cx, cx.evt_empty(e), ((kind_idx / kEvents) & 1u) ^ 1u)) {
           evt_bh[e] = bh;
           tc::mbar_arrive(cx.evt_full(e));
         }
-        ++ev_cnt;
       }
-    } else if (team == 0) {
+    } else if (role == 0) {
       // codes item, team 0: V codes of this warp's 16 tokens, transposed to
       // [channel][token] (4-channel lanes); the V scales come with the K tile
       const float4 svs = *reinterpret_cast<const float4*>(hstat + st * (kHstatBytes / 4) + kHeadDim + 4 * lane);
