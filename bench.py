@@ -59,6 +59,13 @@ def attention_traffic():
     return ATTN_TRAFFIC["bytes"] if digest.startswith(ATTN_TRAFFIC["source_sha256"]) else None
 
 
+def prologue_bytes(B, H, S, D):
+    """Algorithmic prologue bytes: bf16 Q, K, V read once; int8 Q/K and e4m3 V
+    codes, the scales and the key mean written once."""
+    s_pad = -(-S // 128) * 128
+    return 6 * B * S * H * D + 3 * B * H * s_pad * D + 2 * 4 * B * H * (s_pad // 32) + 2 * 4 * B * H * D
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -383,6 +390,24 @@ def run_gpu(args):
     t_pro64 = graph_time(lambda: quantize(q64, k64, v64, "NHD", True, out=qz64))
     t_att64 = graph_time(lambda: attention(qz64, sm64, out=out64))
     del q64, k64, v64, qz64, out64
+    # the other sizes the prologue and attention are measured at (the video
+    # workload at a quarter and at eight times the benchmark's length)
+    other_configs = []
+    p_att_other = attention_peak(peaks)[0]
+    for name in ("B1_H28_S4096", "B1_H28_S131072"):
+        wo = WORKLOADS[name]
+        qo, ko, vo = make_qkv(wo, "cuda")
+        qzo = alloc_bundle(wo.B, wo.S, wo.H, qo.device)
+        outo = torch.empty_like(qo)
+        t_po = graph_time(lambda: quantize(qo, ko, vo, "NHD", wo.smooth_k, out=qzo))
+        t_ao = graph_time(lambda: attention(qzo, sm, out=outo))
+        pb = prologue_bytes(wo.B, wo.H, wo.S, 128)
+        other_configs.append({"workload": name, "attention_ms": t_ao * 1e3,
+                              "attention_tflops": float(wo.attention_ops) / t_ao / 1e12,
+                              "attention_frac_of_peak": float(wo.attention_ops) / t_ao / 1e12 / p_att_other,
+                              "prologue_ms": t_po * 1e3, "prologue_gbs": pb / t_po / 1e9,
+                              "prologue_frac_of_hbm": pb / t_po / 1e9 / peaks["hbm_gbs"]})
+        del qo, ko, vo, qzo, outo
     if device_error() != 0:
         raise RuntimeError("device error word set during timing")
     short_calls = short_call_latency(torch, sageattn, sm) if rank == 0 else None
@@ -417,9 +442,7 @@ def run_gpu(args):
 
     n_elem = B * S * H * D
     s_pad = -(-S // 128) * 128
-    # algorithmic prologue bytes: bf16 Q, K, V read once; int8 Q/K and e4m3 V
-    # codes, the scales and the key mean written once
-    pro_bytes = 6 * n_elem + 3 * B * H * s_pad * D + 2 * 4 * B * H * (s_pad // 32) + 2 * 4 * B * H * D
+    pro_bytes = prologue_bytes(B, H, S, D)
     # sage_quantize also writes the fp16 copies of the Q/K codes the tensor
     # cores read (sm_103a has no int8 MMA kind)
     pro_moved = pro_bytes + 4 * B * H * s_pad * D
@@ -458,6 +481,7 @@ def run_gpu(args):
                         "prologue_ms": t_pro64 * 1e3,
                         "prologue_gbs": 9 * w64.B * w64.H * w64.S * 64 / t_pro64 / 1e9,
                         "prologue_frac_of_hbm": 9 * w64.B * w64.H * w64.S * 64 / t_pro64 / 1e9 / peaks["hbm_gbs"]},
+        "other_configs": other_configs,
         "short_calls": short_calls,
         "e2e": {"value": world * ops / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": 3 * 2 * n_elem,
                 "d2h_bytes_per_step": 2 * n_elem, "ms_per_step": t_e2e * 1e3,
