@@ -74,7 +74,7 @@ enum {
   SAGE_ERR_CAUSAL = -1,         /* is_causal != 0 (no mask support) */
   SAGE_ERR_LSE = -2,            /* return_lse != 0 */
   SAGE_ERR_DTYPE = -3,          /* an input or output is not BF16 */
-  SAGE_ERR_HEAD_DIM = -4,       /* D != 128 */
+  SAGE_ERR_HEAD_DIM = -4,       /* D != 128 (D = 64 is also taken by the bundle entries and sage_sageattn_ex) */
   SAGE_ERR_SHAPE = -5,          /* Q, K, V shapes differ, or a size is negative */
   SAGE_ERR_LAYOUT = -6,         /* tensor_layout is neither "NHD" nor "HND", or channel stride != 1 */
   SAGE_ERR_ALIGN = -7,          /* a base pointer is not 16-byte aligned, or a stride is not a multiple of 8 elements */
@@ -104,13 +104,13 @@ typedef struct sage_bf16_tensor {
 } sage_bf16_tensor;
 
 /* The quantized bundle written by sage_quantize and read by sage_attention.
- * All pointers are device pointers, 16-byte aligned.
- *   q_codes, k_codes : int8   [B][H][S_pad][128]   (rows S..S_pad-1 are 0)
- *   vt_codes         : e4m3fn [B][H][128][S_pad]   (V transposed; cols S..S_pad-1 are 0)
+ * All pointers are device pointers, 16-byte aligned. D = 128 (or 64).
+ *   q_codes, k_codes : int8   [B][H][S_pad][D]     (rows S..S_pad-1 are 0)
+ *   vt_codes         : e4m3fn [B][H][D][S_pad]     (V transposed; cols S..S_pad-1 are 0)
  *   q_scale, k_scale : float  [B][H][S_pad/32]     (blocks past ceil(S/32) are 0)
- *   v_scale          : float  [B][H][128]
- *   k_mean           : float  [B][H][128]          (0 when smooth_k is off)
- *   q16, k16         : fp16   [B][H][S_pad][128]   the same Q and K codes as fp16
+ *   v_scale          : float  [B][H][D]
+ *   k_mean           : float  [B][H][D]            (0 when smooth_k is off)
+ *   q16, k16         : fp16   [B][H][S_pad][D]     the same Q and K codes as fp16
  *                      values (exact: |code| <= 127). sm_103a has no integer
  *                      tensor-core MMA, so the attention kernel multiplies the
  *                      codes on the fp16 tensor cores; writing them once here
@@ -158,7 +158,8 @@ SAGE_API int sage_host_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D
 
 /* The quantization prologue ("prepare"): optional smooth_k key mean (fp64
  * sum), INT8 Q/K per 32-token block, e4m3 V per channel, V stored transposed.
- * q, k, v: BF16 tensors of shape (B, S, H, 128) with the given strides.
+ * q, k, v: BF16 tensors of shape (B, S, H, D), D = 128 or 64, with the given
+ * strides.
  * scratch_dev: at least sage_quantize_scratch_size bytes, 256-byte aligned;
  * its contents on entry do not matter and are clobbered.
  * Enqueued (D = 128): for S > 1024, a clear of the scratch header (work
@@ -205,7 +206,10 @@ SAGE_API int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_te
  * which is exact for |code| <= 127 and 128 channels), dequantization by
  * s_q * s_k * sm_scale, online fp32 softmax, P -> e4m3, FP8 PV on tcgen05
  * with fp32 accumulation in tensor memory, V scales in the epilogue.
- * out: BF16 (B, S, H, 128) at out_dev with element strides (ob, os, oh),
+ * Without the causal mask, at D = 128 and from 16 key tiles (S > 1920) the
+ * kernel runs with a fourth warpgroup that rescales the output accumulator
+ * (512 threads per CTA, else 384); results are the same either way.
+ * out: BF16 (B, S, H, D) at out_dev with element strides (ob, os, oh),
  * channel stride 1. sm_scale must be finite and > 0.
  * The kernel is launched as a programmatic dependent of the previous kernel
  * on the stream: it may start while that kernel (normally the prologue)

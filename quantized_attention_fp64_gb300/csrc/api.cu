@@ -596,7 +596,7 @@ const char* sage_strerror(int code) {
     case SAGE_ERR_CAUSAL: return "is_causal is not supported (non-causal attention only)";
     case SAGE_ERR_LSE: return "return_lse is not supported";
     case SAGE_ERR_DTYPE: return "inputs and output must be bfloat16";
-    case SAGE_ERR_HEAD_DIM: return "head dimension must be 128";
+    case SAGE_ERR_HEAD_DIM: return "head dimension must be 128 (or 64 on the entries that take it)";
     case SAGE_ERR_SHAPE: return "q, k and v must have identical, non-negative shapes";
     case SAGE_ERR_LAYOUT: return "tensor_layout must be \"NHD\" or \"HND\" with a unit channel stride";
     case SAGE_ERR_ALIGN: return "pointers must be 16-byte aligned and strides multiples of 8 elements";
