@@ -64,6 +64,21 @@ def test_attention_ex_matches_oracle(sage_lib, s_len, causal):
     _check(to_np(out), lse.cpu().numpy(), q, k, v, "NHD", ref, causal, [(0, 0), (0, 1)])
 
 
+@pytest.mark.parametrize("s_len", [2048, 2200])
+def test_lse_with_correction_warpgroup(sage_lib, s_len):
+    # unmasked rows of 16 key tiles or more run the kernel with the correction
+    # warpgroup; the log-sum-exp comes from the same softmax state
+    w = custom(1, 2, s_len, seed_index=850 + s_len, k_offset_std=2.0)
+    q, k, v = make_qkv(w, "cuda")
+    qz = quantize(q, k, v, "NHD", True)
+    out, lse = attention(qz, SM, is_causal=False, return_lse=True)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    ref = quantize_tensors(to_np(q), to_np(k), to_np(v), "NHD", True)
+    rows = np.unique(np.concatenate([np.arange(0, s_len, 29), np.arange(s_len - 3, s_len)]))
+    _check(to_np(out), lse.cpu().numpy(), q, k, v, "NHD", ref, False, [(0, 0), (0, 1)], rows=rows)
+
+
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
 def test_sageattn_ex_causal_lse_with_smooth_k_term(sage_lib, layout):
     w = WORKLOADS["B2_H8_S1024"]
