@@ -16,8 +16,6 @@ import test_oracle_causal_lse as C
 import test_oracle_formats as F
 import test_oracle_prologue as P
 
-ORIG_INT8 = so.quantize_int8_blocks
-ORIG_V = so.quantize_v_channels
 ORIG_MEAN = so.key_mean_fp64
 ORIG_EXACT = so.attention_exact
 ORIG_EMU = so.attention_emulated
@@ -175,3 +173,51 @@ def test_causal_mask_off_by_one_is_caught(monkeypatch):
 def test_lse_without_the_smooth_k_term_is_caught(monkeypatch):
     monkeypatch.setattr(C, "smooth_k_lse_term", lambda q, mean, sm, rows=None: np.zeros(np.asarray(q).shape[0]))
     _fails(C.test_emulated_lse_needs_and_gets_the_smooth_k_term, False)
+
+
+def test_p_stored_without_its_448_scale_is_caught(monkeypatch):
+    # the emulation reads the P scale from the oracle module at call time
+    monkeypatch.setattr(so, "P_SCALE", 1.0)
+    _fails(A.test_emulation_single_tile_closed_form)
+
+
+def _emulated_plain(qc, kc, vv, sq, sk, sv, sm, quantize_p=True, return_fp32=False, drop_alpha=False):
+    """A plain copy of the emulation's loop (unmasked, all rows), with an
+    optional planted mistake: the accumulator not rescaled by alpha."""
+    f32, f64 = np.float32, np.float64
+    qc, kc = np.asarray(qc), np.asarray(kc)
+    s_len, d = kc.shape
+    sq = np.asarray(sq, f32)[np.arange(qc.shape[0]) // 32]
+    sk, sv, vv, scale = np.asarray(sk, f32), np.asarray(sv, f32), np.asarray(vv, f32), f32(sm)
+    m = np.full(qc.shape[0], -np.inf, f32)
+    l = np.zeros(qc.shape[0], f32)
+    acc = np.zeros((qc.shape[0], d), f32)
+    for j0 in range(0, s_len, 128):
+        j1 = min(j0 + 128, s_len)
+        s_ij = qc.astype(f64) @ kc[j0:j1].astype(f64).T
+        c = ((sq[:, None] * sk[np.arange(j0, j1) // 32][None, :]).astype(f32) * scale).astype(f32)
+        logit = (s_ij.astype(f32) * c).astype(f32)
+        m_new = np.maximum(m, logit.max(axis=1))
+        alpha = np.exp((m - m_new).astype(f64)).astype(f32)
+        alpha = np.where(m == m_new, f32(1.0), alpha).astype(f32)
+        p = np.exp((logit - m_new[:, None]).astype(f32).astype(f64)).astype(f32)
+        l = (alpha * l + p.astype(f64).sum(axis=1).astype(f32)).astype(f32)
+        p448 = (f32(448.0) * p).astype(f32)
+        p_used = so.e4m3_decode(so.e4m3_encode(p448)) if quantize_p else p448
+        pv = (p_used.astype(f64) @ vv[j0:j1].astype(f64)).astype(f32)
+        acc = ((acc if drop_alpha else alpha[:, None] * acc) + pv).astype(f32)
+        m = m_new
+    out = ((((acc / l[:, None]).astype(f32)) * sv[None, :]).astype(f32) / f32(448.0)).astype(f32)
+    return out if return_fp32 else so.bf16_round(out)
+
+
+def test_accumulator_not_rescaled_by_alpha_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "attention_emulated",
+                        lambda *a, **kw: _emulated_plain(*a, drop_alpha=True, **kw))
+    _fails(A.test_emulation_reduces_to_exact_without_quantization, 300)
+
+
+def test_the_planted_emulation_copy_is_faithful_without_a_mistake(monkeypatch):
+    monkeypatch.setattr(A, "attention_emulated", lambda *a, **kw: _emulated_plain(*a, **kw))
+    A.test_emulation_reduces_to_exact_without_quantization(300)
+    A.test_emulation_scale_indexing()
