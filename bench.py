@@ -239,9 +239,9 @@ def run_profile(args):
     q, k, v = make_qkv(w, "cuda")
     for _ in range(args.warmup + 1):
         qz = quantize(q, k, v, "NHD", w.smooth_k)
-        attention(qz, 1.0 / math.sqrt(128.0))
+        attention(qz, 1.0 / math.sqrt(128.0), is_causal=args.causal)
     torch.cuda.synchronize()
-    print(f"profiled {args.workload}")
+    print(f"profiled {args.workload}" + (" (causal)" if args.causal else ""))
     return 0
 
 
@@ -513,6 +513,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true", help="run one prologue + attention on --workload and exit")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--causal", action="store_true", help="with --profile: the attention call with the causal mask")
     args = ap.parse_args()
     if args.profile:
         return run_profile(args)
