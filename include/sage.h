@@ -158,6 +158,9 @@ SAGE_API int sage_host_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D
 
 /* The quantization prologue ("prepare"): optional smooth_k key mean (fp64
  * sum), INT8 Q/K per 32-token block, e4m3 V per channel, V stored transposed.
+ * Defined by "aiter-sage-attention ... #1222", section "The kernel" (the
+ * per-block and per-channel quantization), and "Hand-written prologue ...
+ * (v0.4.0)", section "What changed" (the fp64 key mean, 64-bit offsets).
  * q, k, v: BF16 tensors of shape (B, S, H, D), D = 128 or 64, with the given
  * strides.
  * scratch_dev: at least sage_quantize_scratch_size bytes, 256-byte aligned;
@@ -201,7 +204,8 @@ SAGE_API int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_te
                                    const sage_bf16_tensor* v, int64_t B, int64_t S, int64_t H, int64_t D,
                                    int smooth_k, const sage_quantized* out, void* cuda_stream);
 
-/* The attention kernel on a quantized bundle: INT8 QK^T with exact integer
+/* The attention kernel on a quantized bundle ("aiter-sage-attention ...
+ * #1222", section "The kernel"): INT8 QK^T with exact integer
  * accumulation (run on the tcgen05 tensor cores as fp16 x fp16 -> fp32,
  * which is exact for |code| <= 127 and 128 channels), dequantization by
  * s_q * s_k * sm_scale, online fp32 softmax, P -> e4m3, FP8 PV on tcgen05
@@ -257,8 +261,9 @@ SAGE_API int sage_attention_simt(const sage_quantized* in, int64_t B, int64_t S,
                         float sm_scale, int is_causal, void* out_dev, int64_t ob, int64_t os, int64_t oh,
                         float* lse_dev, void* cuda_stream);
 
-/* The sageattn-shaped entry: quantize q, k, v into the workspace, then run
- * attention into out. Shapes and strides are given in the order of
+/* The sageattn-shaped entry ("aiter-sage-attention ... #1222", section "What
+ * I have so far"): quantize q, k, v into the workspace, then run attention
+ * into out. Shapes and strides are given in the order of
  * tensor_layout: "NHD" = [B, S, H, D], "HND" = [B, H, S, D]; strides are in
  * elements. out has q's shape with out_strides.
  * sm_scale: NaN selects 1/sqrt(D); otherwise it must be finite and > 0.
