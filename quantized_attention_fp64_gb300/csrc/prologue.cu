@@ -8,15 +8,16 @@
 // opt-in (v0.4.0)", section "What changed" (64-bit offsets; key mean summed
 // in fp64).
 //
-// One persistent kernel, one CTA per SM: two teams of 8 compute warps and 1
-// TMA producer warp. The work is a list of items claimed in order from a
-// global counter:
+// One persistent kernel, one CTA per SM: two teams of 8 compute warps (they
+// swap roles from one item to the next), a TMA producer warp and a counter
+// warp. The work is a list of items claimed in order from a global counter:
 //   stats item (head, 128-token group): Q codes and scales; exact fp64 key
 //     sums of the group (4 chunks of 32 tokens, then a 2-level pairwise tree);
-//     the group's max |v| per channel. The last stats item of a head (counted
-//     with an atomic) finishes that head: the pairwise tree over its group sums
-//     gives the key mean, the max over groups the V scales; then it publishes
-//     the head as ready.
+//     the group's max |v| per channel. The counter warp counts each finished
+//     group with an atomic per head; the CTA that counts a head's last group
+//     finishes that head (team 1, on a finish marker the producer puts in the
+//     ring): the pairwise tree over its group sums gives the key mean, the max
+//     over groups the V scales; then it publishes the head as ready.
 //   codes item (head, 128-token group): K codes of k - mean, V codes
 //     (transposed); the producer loads its tiles once the head is ready.
 // All stats items come before all codes items (the general order, codes of
@@ -44,7 +45,7 @@
 // (quantize_half_block). For e4m3, rounding is monotone, so when
 // q = fl(v*fl(1/s)) scaled by (1 - 2^-21) and by (1 + 2^-21) round to the same
 // code, fl(v/s) (within 2^-22 relative of q) does too; otherwise the exact
-// division decides (v_code_quad). Q and V maxima are taken on the bf16 bit
+// division decides (v_code_quad_fast, exact_v_quad). Q and V maxima are taken on the bf16 bit
 // patterns, whose magnitudes order as integers.
 #include <cuda_fp16.h>
 
