@@ -330,6 +330,14 @@ SAGE_API int sage_sageattn_host(const void* q_host, const void* k_host, const vo
  * or CUDA. */
 SAGE_API int sage_device_error(void* cuda_stream, int* code);
 
+/* Test support for the bounded waits: enqueues on cuda_stream one kernel
+ * whose only warp waits, with the bounded wait every kernel of the library
+ * uses, on an internal barrier that nothing ever completes. When the wait's
+ * limit (2 s) runs out the kernel sets the device error word and returns;
+ * sage_device_error then reports SAGE_ERR_DEVICE_TIMEOUT, and the context
+ * remains usable. Nothing else is touched. Returns SAGE_OK, ARCH or CUDA. */
+SAGE_API int sage_selftest_wait_timeout(void* cuda_stream);
+
 /* Static description of an error code; never NULL. */
 SAGE_API const char* sage_strerror(int code);
 

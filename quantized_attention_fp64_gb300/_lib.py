@@ -55,6 +55,7 @@ _SIGNATURES = {
     "sage_sageattn_host": (c_int, [c_vp, c_vp, c_vp, I64x4, c_int, ctypes.c_char_p, c_int, ctypes.c_float, c_int, c_vp,
                                    c_int, c_vp, ctypes.c_size_t, c_vp]),
     "sage_device_error": (c_int, [c_vp, ctypes.POINTER(c_int)]),
+    "sage_selftest_wait_timeout": (c_int, [c_vp]),
     "sage_strerror": (ctypes.c_char_p, [c_int]),
 }
 

@@ -590,6 +590,13 @@ int sage_device_error(void* cuda_stream, int* code) {
   return SAGE_OK;
 }
 
+int sage_selftest_wait_timeout(void* cuda_stream) {
+  int dev = 0;
+  const int rc = check_device(&dev);
+  if (rc != SAGE_OK) return rc;
+  return cuda_status(launch_wait_timeout_selftest(g_err_ptr[dev], static_cast<cudaStream_t>(cuda_stream)));
+}
+
 const char* sage_strerror(int code) {
   switch (code) {
     case SAGE_OK: return "success";

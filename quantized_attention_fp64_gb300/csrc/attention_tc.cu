@@ -809,6 +809,26 @@ __global__ void __launch_bounds__(threads_of<kCorr>(), 1)
   }
 }
 
+// The bounded wait put to the test: the only warp waits on a barrier that
+// nothing arrives on (phase 0 of a fresh mbarrier never completes); after the
+// wait's limit it flags the device error word and the kernel ends, with the
+// context still usable.
+__global__ void __launch_bounds__(32, 1) wait_timeout_selftest_kernel(int* dev_err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  Ctx cx;
+  cx.bar0 = tc::smem_u32(&bar);
+  cx.abort_flag = reinterpret_cast<volatile int*>(&abort_flag);
+  cx.dev_err = dev_err;
+  if (threadIdx.x == 0) {
+    *cx.abort_flag = 0;
+    tc::mbar_init(cx.bar(0), 1);
+    tc::fence_mbar_init();
+  }
+  __syncwarp();
+  wait_bar_warp(cx, cx.bar(0), 0);
+}
+
 // 3-D tensor [d2][d1][d0] of `esize`-byte elements; boxes of box0 x box1 x 1
 // elements with the 128-byte swizzle (box0 * esize must be 128).
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base, uint64_t d0, uint64_t d1,
@@ -870,6 +890,11 @@ const Sched* causal_schedule(int64_t n_units, int64_t pairs, int64_t n_kv, int g
 }
 
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(int* dev_err, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(dev_err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
                                 const Out& out, bool causal, float* lse, int* dev_err, cudaStream_t stream) {

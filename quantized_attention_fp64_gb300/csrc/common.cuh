@@ -85,6 +85,11 @@ cudaError_t launch_attention_simt(const Bundle& in, int64_t B, int64_t S, int64_
 cudaError_t launch_attention_tc(const Bundle& in, int64_t B, int64_t S, int64_t H, int64_t D, float sm_scale,
                                 const Out& out, bool causal, float* lse, int* dev_err, cudaStream_t stream);
 
+// Test of the bounded wait: one warp waits, with the attention kernel's
+// bounded wait, on an mbarrier that nothing completes; when the wait runs out
+// the kernel sets *dev_err and returns.
+cudaError_t launch_wait_timeout_selftest(int* dev_err, cudaStream_t stream);
+
 // Adds sm_scale * q_i . k_mean to lse[b][h][i] (the smooth_k term that turns
 // the log-sum-exp of the mean-reduced keys into that of the original keys).
 cudaError_t launch_lse_smooth_k_term(const Bf16In& q, const float* k_mean, int64_t B, int64_t S, int64_t H,
