@@ -224,3 +224,13 @@ def test_host_workspace_size_grows_with_groups_in_flight(lib):
     assert one > auto
     assert lib.sage_host_workspace_size(1, 16384, 28, 128, -1, ctypes.byref(n)) == ARG
     assert lib.sage_host_workspace_size(1, 16384, 28, 96, 0, ctypes.byref(n)) == HEAD_DIM
+
+
+def test_device_entries_without_a_device_return_an_error(lib):
+    # no GPU in this process: the entries that need one report an error
+    # code (a failed CUDA call) instead of crashing or launching anything
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    code = ctypes.c_int(0)
+    assert lib.sage_selftest_wait_timeout(None) < 0
+    assert lib.sage_device_error(None, ctypes.byref(code)) < 0
