@@ -461,9 +461,11 @@ __device__ __forceinline__ bool v_code_quad_fast(uint2 w, float2 r01, float2 r23
 // Exact fp64 sums of one 32-token key chunk, by the two warps of a pair
 // (sub 0 and 1, 16 rows each; rows: this warp's rows, read with 8-channel
 // lanes; nv: its rows below S; nvc: the chunk's rows below S). The second
-// half posts its float pairs and magnitude bounds in xk_*; the first half
-// joins them, replaces the result by the left-to-right fp64 sums when the
-// pair sums may be inexact, and writes the chunk's 128 sums to ks_chunk.
+// half posts its float pairs and, per lane, the magnitude bounds of the
+// lane's 8 channels in xk_*; the first half joins them, replaces the result
+// by the left-to-right fp64 sums when the pair sums of a lane's channels may
+// be inexact (judged on both halves' bounds for those channels), and writes
+// the chunk's 128 sums to ks_chunk.
 // `release` runs once the warp has stopped reading its rows.
 template <typename Release>
 __device__ __forceinline__ void key_chunk_sums(const uint8_t* rows, int nv, int nvc, int sub, int lane, int pair,
@@ -485,9 +487,10 @@ __device__ __forceinline__ void key_chunk_sums(const uint8_t* rows, int nv, int 
         xk_lo[8 * lane + 2 * k + 1] = lo[k].y;
       }
     }
-    if (lane == 0) {
-      xk_bits[0] = mx;
-      xk_bits[1] = mn;
+    if (lane < 16) {
+      // the bounds of this lane's 8 channels (lanes l and l + 16 hold the same)
+      xk_bits[lane] = mx;
+      xk_bits[16 + lane] = mn;
     }
     pair_bar(pair);
     release();
@@ -504,7 +507,7 @@ __device__ __forceinline__ void key_chunk_sums(const uint8_t* rows, int nv, int 
     sums[2 * k] = __dadd_rn(static_cast<double>(s.x), static_cast<double>(l.x));
     sums[2 * k + 1] = __dadd_rn(static_cast<double>(s.y), static_cast<double>(l.y));
   }
-  if (!key_sum_exact(__vmaxu2(mx, xk_bits[0]), __vminu2(mn, xk_bits[1]))) {
+  if (!key_sum_exact(__vmaxu2(mx, xk_bits[lane & 15]), __vminu2(mn, xk_bits[16 + (lane & 15)]))) {
     // this warp's rows are followed by the second half's in the tile
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) sums[c] = fp64_chunk_sum(rows, nvc, (lane & 15) * 16 + 2 * c);
@@ -739,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ double ks[kTeams][kChunks][kHeadDim];            // exact chunk sums
   __shared__ uint32_t vm[kTeams][kWarps][kHeadDim / 2];       // per-warp max |v| bits, channel pairs
   __shared__ float xk_hi[kTeams][kChunks][kHeadDim], xk_lo[kTeams][kChunks][kHeadDim];  // second-half key sums
-  __shared__ uint32_t xk_bits[kTeams][kChunks][2];            // second-half magnitude bounds
+  __shared__ uint32_t xk_bits[kTeams][kChunks][32];           // second-half magnitude bounds per lane
   __shared__ float xa[2][kTeams * kWarps / 2][2];     // amax of each half block, two parities
   __shared__ float fin_vmax[kHeadDim];
   __shared__ double fin_right[kHeadDim];
@@ -1162,7 +1165,7 @@ __global__ void __launch_bounds__(kShortThreads, 1)
   __shared__ double ks[kChunks][kHeadDim];       // exact chunk sums of this group
   __shared__ uint32_t vm[kWarps][kHeadDim / 2];  // per-warp max |v| bits, channel pairs
   __shared__ float xk_hi[kChunks][kHeadDim], xk_lo[kChunks][kHeadDim];  // second-half key sums
-  __shared__ uint32_t xk_bits[kChunks][2];       // second-half magnitude bounds
+  __shared__ uint32_t xk_bits[kChunks][32];      // second-half magnitude bounds per lane
   __shared__ float xa[kTeams * kWarps / 2][2];   // block amax exchange of each warp pair
   __shared__ double g_sum[kShortMaxGroups][kHeadDim];    // every group's key sums (stored by the cluster)
   __shared__ uint32_t g_max[kShortMaxGroups][kHeadDim];  // every group's max |v| bits

@@ -49,12 +49,15 @@ def test_prologue_long_sequence_sampled_heads(sage_lib):
     _run(q, k, v, "NHD", True, heads=[(0, 0), (0, 13), (0, 27)])
 
 
-def test_prologue_edge_values(sage_lib):
+@pytest.mark.parametrize("S", [300, 1300])
+def test_prologue_edge_values(sage_lib, S):
     """Zero blocks and channels, negative zeros, bf16 subnormals, exact .5
     ties of x/s, a key chunk whose fp64 sum rounds (forcing the exact fp64
-    path) and huge magnitudes."""
+    path) and huge magnitudes; S = 300 runs the cluster kernel, S = 1300 the
+    persistent one (whose head key sums then take the pairwise tree over the
+    group sums)."""
     rng = np.random.default_rng(5)
-    S, H = 300, 2
+    H = 2
     q = rng.standard_normal((1, S, H, 128)).astype(np.float32)
     k = rng.standard_normal((1, S, H, 128)).astype(np.float32) + 3.0
     v = rng.standard_normal((1, S, H, 128)).astype(np.float32)
@@ -78,12 +81,14 @@ def test_prologue_edge_values(sage_lib):
         _run(qt, kt, vt, "NHD", smooth)
 
 
-def test_prologue_key_sum_exponent_spread(sage_lib):
+@pytest.mark.parametrize("S", [1000, 2100])
+def test_prologue_key_sum_exponent_spread(sage_lib, S):
     """Key chunks whose magnitudes span 20 to 50 binades, so that both the
     float-pair chunk sums and the fp64 fallback run, with cancelling signs and
-    ragged chunks; the key mean and every code must still match bit for bit."""
+    ragged chunks; the key mean and every code must still match bit for bit
+    (S = 1000: the cluster kernel; S = 2100: the persistent kernel)."""
     rng = np.random.default_rng(11)
-    S, H = 1000, 3
+    H = 3
     q = rng.standard_normal((1, S, H, 128)).astype(np.float32)
     k = rng.standard_normal((1, S, H, 128)).astype(np.float32)
     v = rng.standard_normal((1, S, H, 128)).astype(np.float32)
@@ -101,3 +106,26 @@ def test_prologue_key_sum_exponent_spread(sage_lib):
     qt, kt, vt = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (q, k, v))
     _run(qt, kt, vt, "NHD", True)
     _run(qt, kt, vt, "NHD", False)
+
+
+@pytest.mark.parametrize("S", [256, 2048])
+def test_prologue_chunk_bounds_second_half(sage_lib, S):
+    """A key chunk whose exponent spread sits only in the second half of its
+    32 tokens, in channels past the first 8: tokens 16, 18, 20 of the chunk
+    hold 1, 2^-24 and 2^-52 in one channel that is zero elsewhere. The
+    float-pair chunk sum loses the 2^-52 (its error term rounds), the
+    left-to-right fp64 sum keeps it, and the key mean fl32(T / S) then sits
+    just above an fp32 tie instead of on it; each warp's exactness test must
+    use the bounds of its own channels from the other half's rows."""
+    rng = np.random.default_rng(23)
+    H = 2
+    q = rng.standard_normal((1, S, H, 128)).astype(np.float32)
+    k = rng.standard_normal((1, S, H, 128)).astype(np.float32)
+    v = rng.standard_normal((1, S, H, 128)).astype(np.float32)
+    for h, c, chunk in ((0, 8, 0), (1, 77, 5)):
+        t0 = 32 * chunk + 16
+        k[0, :, h, c] = 0.0
+        k[0, t0, h, c], k[0, t0 + 2, h, c], k[0, t0 + 4, h, c] = 1.0, 2.0 ** -24, 2.0 ** -52
+    dev = torch.device("cuda")
+    qt, kt, vt = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (q, k, v))
+    _run(qt, kt, vt, "NHD", True)
