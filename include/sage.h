@@ -188,10 +188,15 @@ SAGE_API int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k,
  * sums go to a 32 MiB device array built into the library, which every GPU
  * that loads the library holds until the process exits. The web pages this
  * library follows have no counterpart to this entry point.
- * Limit: the problem must need at most 32 MiB of prologue scratch, i.e.
- * B * H * (ceil(S / 128) * 128 * 12 + 512) bytes (each part rounded up to 256 bytes)
- * <= 32 MiB, about 21 800 (head, 128-token group) pairs; larger problems are
- * rejected with SAGE_ERR_WORKSPACE and nothing is launched.
+ * Limit: where the prologue uses scratch, it must need at most 32 MiB of it:
+ * sage_quantize_scratch_size(B, S, H, D) <= 32 MiB. That is about
+ * B * H * (S_pad * 12 + 512) bytes at D = 128 (about 21 800 (head,
+ * 128-token group) pairs) and B * H * S_pad * 24 bytes at D = 64 (about
+ * 10 900 pairs), with S_pad = ceil(S / 128) * 128; larger problems are
+ * rejected with SAGE_ERR_WORKSPACE and nothing is launched. At D = 128 with
+ * S <= 1024 the prologue runs as one cluster kernel that uses no scratch, so
+ * there the limit does not apply (only the library's general size limits,
+ * SAGE_ERR_TOO_LARGE, as for sage_quantize).
  * The first call on each device looks up the array's device address with
  * cudaGetSymbolAddress; make that first call before any stream capture.
  * All calls share the array and it keeps the last call's contents; each call

@@ -14,6 +14,20 @@
 #include "common.cuh"
 
 namespace sage {
+// The size limits every entry point applies (offsets stay within 64-bit
+// arithmetic, work-item counters within 32 bits).
+int check_problem_sizes(int64_t B, int64_t S, int64_t H, int64_t D) {
+  constexpr int64_t kMaxBH = 65535;
+  constexpr int64_t kMaxS = int64_t(1) << 31;
+  constexpr int64_t kMaxElems = int64_t(1) << 44;
+  if (B < 0 || S < 0 || H < 0 || D < 0) return SAGE_ERR_SHAPE;
+  if (D != kHeadDim && D != 64) return SAGE_ERR_HEAD_DIM;
+  if (B > kMaxBH || H > kMaxBH || S > kMaxS) return SAGE_ERR_TOO_LARGE;
+  if (B * H > kMaxBH * 16) return SAGE_ERR_TOO_LARGE;
+  if (B * H * padded_len(S) > kMaxElems / D) return SAGE_ERR_TOO_LARGE;
+  return SAGE_OK;
+}
+
 namespace {
 
 // Set by kernels that give up a bounded wait; read and cleared by
@@ -53,14 +67,7 @@ int check_device(int* dev_out) {
   return SAGE_OK;
 }
 
-int check_sizes(int64_t B, int64_t S, int64_t H, int64_t D) {
-  if (B < 0 || S < 0 || H < 0 || D < 0) return SAGE_ERR_SHAPE;
-  if (D != kHeadDim && D != 64) return SAGE_ERR_HEAD_DIM;
-  if (B > kMaxBH || H > kMaxBH || S > kMaxS) return SAGE_ERR_TOO_LARGE;
-  if (B * H > kMaxBH * 16) return SAGE_ERR_TOO_LARGE;
-  if (B * H * padded_len(S) > kMaxElems / D) return SAGE_ERR_TOO_LARGE;
-  return SAGE_OK;
-}
+int check_sizes(int64_t B, int64_t S, int64_t H, int64_t D) { return check_problem_sizes(B, S, H, D); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride_ok(int64_t s) { return s % 8 == 0; }

@@ -75,6 +75,12 @@ size_t prologue64_scratch_bytes(int64_t B, int64_t S, int64_t H);
 // or nullptr if the runtime call fails.
 int* device_error_ptr();
 size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H, int64_t D);
+// Whether launch_prologue touches its scratch for this shape (the cluster
+// kernel of short sequences at D = 128 does not).
+bool prologue_uses_scratch(int64_t S, int64_t D);
+// The size limits every entry point applies: SAGE_OK or a negative SAGE_ERR_*
+// code (SHAPE, HEAD_DIM, TOO_LARGE).
+int check_problem_sizes(int64_t B, int64_t S, int64_t H, int64_t D);
 
 cudaError_t launch_attention_simt(const Bundle& in, int64_t B, int64_t S, int64_t H, float sm_scale,
                                   const Out& out, bool causal, float* lse, cudaStream_t stream);

@@ -1387,6 +1387,10 @@ int make_input_map(CUtensorMap* m, const Bf16In& t, int64_t B, int64_t S, int64_
 
 }  // namespace
 
+bool prologue_uses_scratch(int64_t S, int64_t D) {
+  return D != kHeadDim || div_up(S, kItemTokens) > kShortMaxGroups;
+}
+
 size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H, int64_t D) {
   return D == kHeadDim ? scratch_layout(B, S, H).total : prologue64_scratch_bytes(B, S, H);
 }

@@ -90,10 +90,8 @@ using namespace sage;
 extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_tensor* k,
                                      const sage_bf16_tensor* v, int64_t B, int64_t S, int64_t H, int64_t D,
                                      int smooth_k, const sage_quantized* out, void* cuda_stream) {
-  if (B < 0 || S < 0 || H < 0 || D < 0) return SAGE_ERR_SHAPE;
-  if (D != kHeadDim && D != 64) return SAGE_ERR_HEAD_DIM;
-  if (B > 65535 || H > 65535 || S > (int64_t(1) << 31)) return SAGE_ERR_TOO_LARGE;
   int rc;
+  if ((rc = check_problem_sizes(B, S, H, D)) != SAGE_OK) return rc;
   if ((rc = check_in(q)) != SAGE_OK || (rc = check_in(k)) != SAGE_OK || (rc = check_in(v)) != SAGE_OK) return rc;
   if (out == nullptr) return SAGE_ERR_NULLPTR;
   const void* ptrs[9] = {out->q_codes_dev, out->k_codes_dev, out->vt_codes_dev, out->q_scale_dev, out->k_scale_dev,
@@ -102,9 +100,11 @@ extern "C" int sage_quantize_noalloc(const sage_bf16_tensor* q, const sage_bf16_
     if (p == nullptr) return SAGE_ERR_NULLPTR;
     if (!aligned16(p)) return SAGE_ERR_ALIGN;
   }
-  // the built-in buffer bounds the problem size: B * H * ceil(S / 128) groups
-  // of 128 channels, 12 bytes each, and 512 bytes per head (plus alignment)
-  if (prologue_scratch_bytes(B, S, H, D) > kNoAllocScratch) return SAGE_ERR_WORKSPACE;
+  // the built-in buffer bounds the problem size where the prologue uses
+  // scratch at all (the cluster kernel of short sequences at D = 128 does
+  // not): its scratch must fit in kNoAllocScratch bytes
+  if (prologue_uses_scratch(S, D) && prologue_scratch_bytes(B, S, H, D) > kNoAllocScratch)
+    return SAGE_ERR_WORKSPACE;
   void* scratch = noalloc_scratch_ptr(&rc);
   if (scratch == nullptr) return rc;
   if (B == 0 || H == 0 || S == 0) return SAGE_OK;
