@@ -73,12 +73,6 @@ def bf16_round(x) -> np.ndarray:
     return out
 
 
-def bf16_bits_to_f32(bits) -> np.ndarray:
-    """Widen raw bfloat16 bit patterns (uint16) to float32 exactly."""
-    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    return b.view(_F32)
-
-
 def _e4m3_value_table() -> np.ndarray:
     """Value of each of the 256 OCP E4M3 ("e4m3fn") codes, from the format.
 
