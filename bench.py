@@ -35,18 +35,21 @@ WORKLOAD = "B1_H28_S16384"
 METRIC = "attention TOPS at B1 H28 S16k D128 (frac of INT8/FP8 peak); prologue HBM GB/s"
 
 
-def bench_config(world=1):
+def bench_config(world=1, strong=False):
     """The workload named in both arms' JSON lines."""
+    par = (f"heads split over {world} ranks (strong scaling, no exchange)" if strong
+           else f"replicas x{world} (heads are independent)")
     return {"workload": WORKLOAD, "B": 1, "H": 28, "S": 16384, "D": 128, "smooth_k": True, "layout": "NHD",
-            "l2": "inputs (3 x 117 MB) larger than L2; no flush",
-            "parallelism": f"replicas x{world} (heads are independent)"}
+            "l2": "step inputs (3 x 117 MB) larger than L2; per-kernel and per-config times with a 2xL2 scrub "
+                  "written before each rep",
+            "parallelism": par}
+
+
 # DRAM traffic of one attention launch at this workload (dram__bytes_read.sum +
-# dram__bytes_write.sum from one ncu capture), valid only for the kernel source
-# it was taken on: reported when the source's SHA-256 prefix still matches.
-# (The file gained the bounded-wait self-test kernel after the capture; the
-# attention kernel's code is unchanged, so the record carries over.)
-ATTN_TRAFFIC = {"bytes": 293938944 + 94170368, "source_sha256": "57fc1970c0a06547",
-                "capture": "ncu --set full, profiles/attention_tc_B1_H28_S16384.md"}
+# dram__bytes_write.sum from one ncu capture of the kernel), with the SHA-256
+# prefix of the kernel's source file the capture was taken on: reported only
+# while the source still matches.
+ATTN_TRAFFIC = {"bytes": 293880320 + 94891520, "source_sha256": "57fc1970c0a06547"}
 PROLOGUE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -202,6 +205,110 @@ def cpu_oracle_sample(rows=1024, seed=3, heads=1):
     }
 
 
+def cold_time(torch, fn, scrub, reps=7):
+    """Median device time of one call of fn with L2 cold: fn is captured in
+    a one-call CUDA graph; before each rep a buffer of twice the L2 size is
+    written (untimed), then CUDA events on the launching stream bracket the
+    graph replay. The scrub keeps the GPU busy while the host enqueues the
+    events and the replay, so no host time falls between them."""
+    import statistics
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    times = []
+    for r in range(reps):
+        scrub.fill_(r & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) / 1e3)
+    return statistics.median(times)
+
+
+# The configurations the pages' workloads are stood in for by (the five
+# synthetic shapes, config 2 with smooth_k on and off) and the 80-head case
+# past 2^31 bytes per tensor: (workload, smooth_k, oracle heads, oracle rows).
+CONFIGS = [("B1_H2_S256", False, 2, 256), ("B2_H8_S1024", True, 4, 256), ("B2_H8_S1024", False, 4, 256),
+           ("B1_H28_S4096", True, 3, 256), ("B1_H28_S16384", True, 3, 256), ("B1_H28_S131072", True, 1, 128),
+           ("B1_H80_S131072", True, 1, 128)]
+
+
+def config_rows(torch, peaks, scrub, sm):
+    """Per configuration: the prologue (sage_quantize) and the attention
+    kernel timed with L2 cold, against the measured peaks; the accuracy of
+    sampled rows of sampled heads against the oracle (its emulation of the
+    quantized method and exact fp64 attention); and the oracle's own time on
+    that sample, extrapolated to the whole configuration."""
+    import numpy as np
+
+    from oracle.tensors import attention_from_codes, exact_head, quantize_tensors
+    from quantized_attention_fp64_gb300 import sageattn
+    from quantized_attention_fp64_gb300.api import alloc_bundle, attention, quantize
+    from quantized_attention_fp64_gb300.workloads import WORKLOADS, make_qkv
+
+    p_att = attention_peak(peaks)[0]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    rows_out = []
+    for name, smooth, n_heads, n_rows in CONFIGS:
+        w = WORKLOADS[name]
+        B, H, S = w.B, w.H, w.S
+        q, k, v = make_qkv(w, "cuda")
+        qz = alloc_bundle(B, S, H, q.device)
+        out = torch.empty_like(q)
+        t_pro = cold_time(torch, lambda: quantize(q, k, v, "NHD", smooth, out=qz), scrub)
+        t_att = cold_time(torch, lambda: attention(qz, sm, out=out), scrub)
+        o = sageattn(q, k, v, sm_scale=sm, smooth_k=smooth)
+        torch.cuda.synchronize()
+        pb = prologue_bytes(B, H, S, 128)
+        ops = float(w.attention_ops)
+        # sampled heads (first, middle, last) and rows (seeded), as host arrays
+        heads = sorted({(bb, hh) for bb, hh in [(0, 0), (B - 1, H - 1), (B // 2, H // 2), (0, H // 3)]})[:n_heads]
+        rows = np.sort(np.random.default_rng(17).choice(S, min(S, n_rows), replace=False))
+        qs, ks, vs = (torch.stack([t[bb, :, hh] for bb, hh in heads], dim=1)[None].float().cpu().numpy()
+                      for t in (q, k, v))
+        got = torch.stack([o[bb, :, hh] for bb, hh in heads], dim=1).float().cpu().numpy()[rows]
+        t0 = time.perf_counter()
+        ref = quantize_tensors(qs, ks, vs, "NHD", smooth)
+        t1 = time.perf_counter()
+        emu = np.stack([attention_from_codes(ref, S, sm, 0, i, rows=rows) for i in range(len(heads))], axis=1)
+        t2 = time.perf_counter()
+        exact = np.stack([exact_head(qs, ks, vs, "NHD", sm, 0, i, rows=rows) for i in range(len(heads))], axis=1)
+        err = np.abs(got.astype(np.float64) - emu)
+
+        def cos(a, b):
+            a, b = np.asarray(a, np.float64).ravel(), np.asarray(b, np.float64).ravel()
+            return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
+
+        n_pairs = len(heads)
+        cpu_full = (t1 - t0) * (B * H / n_pairs) + (t2 - t1) * (B * H * S / (n_pairs * len(rows)))
+        rows_out.append({
+            "workload": name, "smooth_k": smooth,
+            "prologue_ms": t_pro * 1e3, "prologue_gbs": pb / t_pro / 1e9,
+            "prologue_frac_of_hbm": pb / t_pro / 1e9 / peaks["hbm_gbs"],
+            "attention_ms": t_att * 1e3, "attention_tops": ops / t_att / 1e12,
+            "attention_frac_of_peak": ops / t_att / 1e12 / p_att,
+            "accuracy": {"cos_vs_exact": cos(got, exact), "cos_emulation_vs_exact": cos(emu, exact),
+                         "max_abs_vs_emulation": float(err.max()), "mean_abs_vs_emulation": float(err.mean()),
+                         "sample": f"{n_pairs} (batch, head) pairs x {len(rows)} query rows"},
+            "cpu_oracle": {"sample_seconds": t2 - t0, "extrapolated_seconds": cpu_full, "cores": cores,
+                           "sample": f"prologue of {n_pairs} heads + emulated attention of {len(rows)} rows each",
+                           "gpu_speedup": cpu_full / (t_pro + t_att)},
+            "timing": "median of 7, CUDA events around a one-call graph replay, 2xL2 scrub before each rep"})
+        del q, k, v, qz, out, o
+        torch.cuda.empty_cache()
+    return rows_out
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -309,7 +416,7 @@ def short_call_latency(torch, sageattn, sm):
 def run_gpu(args):
     import torch
 
-    from quantized_attention_fp64_gb300 import _build, device_error, sageattn, workspace_size
+    from quantized_attention_fp64_gb300 import _build, device_error, dist, sageattn, workspace_size
     from quantized_attention_fp64_gb300.api import alloc_bundle, attention, quantize
 
     _build.build()
@@ -319,15 +426,28 @@ def run_gpu(args):
 
     w = WORKLOADS[WORKLOAD]
     B, H, S, D = w.B, w.H, w.S, 128
-    ops = float(w.attention_ops)
+    strong = args.strong and world > 1
+    ops_total = float(w.attention_ops)
     q, k, v = make_qkv(w, "cuda")
     out = torch.empty_like(q)
-    ws = torch.empty(workspace_size(B, S, H, D), dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.current_stream()
     sm = 1.0 / math.sqrt(128.0)
+    stream = torch.cuda.current_stream()
+    if strong:
+        # this rank's block of heads (strided views of the full tensors: each
+        # rank holds the whole input, as after a broadcast, and computes its
+        # heads; no exchange)
+        h0, h1 = dist.head_shard(H, rank, world)
+        qb, kb, vb = (dist.head_block(t, rank, world) for t in (q, k, v))
+        out_b = torch.empty((B, S, h1 - h0, D), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(workspace_size(B, S, h1 - h0, D), dtype=torch.uint8, device="cuda")
 
-    def step():
-        sageattn(q, k, v, tensor_layout="NHD", sm_scale=sm, out=out, workspace=ws)
+        def step():
+            sageattn(qb, kb, vb, tensor_layout="NHD", sm_scale=sm, out=out_b, workspace=ws)
+    else:
+        ws = torch.empty(workspace_size(B, S, H, D), dtype=torch.uint8, device="cuda")
+
+        def step():
+            sageattn(q, k, v, tensor_layout="NHD", sm_scale=sm, out=out, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -349,12 +469,16 @@ def run_gpu(args):
     barrier(world)
     t_step = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world)
     clocks = clk.summary()
+    # whole-job attention ops per step: the full workload split over the ranks
+    # (strong), or one workload per rank (weak)
+    job_ops = ops_total if strong else world * ops_total
 
-    # --- per-kernel timing on the launching stream: each kernel group alone,
-    # replayed from a CUDA graph of n_k back-to-back calls so that host-side
-    # launch overhead does not appear in the device time
+    # --- per-kernel timing on the launching stream (the benchmark workload):
+    # each kernel alone, replayed from a CUDA graph of n_k back-to-back calls
+    # (warm: K and V of one head are re-read from L2 by every unit anyway),
+    # and once more with L2 cold (a 2xL2 scrub before each single call)
     qz = alloc_bundle(B, S, H, q.device)
-    scratch = torch.empty(max(1, ws.numel()), dtype=torch.uint8, device="cuda")
+    scratch = torch.empty(max(1, workspace_size(B, S, H, D)), dtype=torch.uint8, device="cuda")
     n_k = max(args.steps, 5)
 
     def graph_time(fn):
@@ -376,8 +500,12 @@ def run_gpu(args):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / 1e3 / n_k
 
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    scrub = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
     t_pro = graph_time(lambda: quantize(q, k, v, "NHD", True, out=qz, scratch=scratch))
     t_att = graph_time(lambda: attention(qz, sm, out=out))
+    t_pro_cold = cold_time(torch, lambda: quantize(q, k, v, "NHD", True, out=qz, scratch=scratch), scrub)
+    t_att_cold = cold_time(torch, lambda: attention(qz, sm, out=out), scrub)
     # the causal mask (sage_attention_ex): the kernel skips the key tiles a
     # query tile cannot see, so it does the visible half of the work
     t_att_causal = graph_time(lambda: attention(qz, sm, out=out, is_causal=True))
@@ -392,26 +520,9 @@ def run_gpu(args):
     t_pro64 = graph_time(lambda: quantize(q64, k64, v64, "NHD", True, out=qz64))
     t_att64 = graph_time(lambda: attention(qz64, sm64, out=out64))
     del q64, k64, v64, qz64, out64
-    # the other sizes the prologue and attention are measured at (the video
-    # workload at a quarter and at eight times the benchmark's length)
-    other_configs = []
-    p_att_other = attention_peak(peaks)[0]
-    for name in ("B1_H28_S4096", "B1_H28_S131072"):
-        wo = WORKLOADS[name]
-        qo, ko, vo = make_qkv(wo, "cuda")
-        qzo = alloc_bundle(wo.B, wo.S, wo.H, qo.device)
-        outo = torch.empty_like(qo)
-        t_po = graph_time(lambda: quantize(qo, ko, vo, "NHD", wo.smooth_k, out=qzo))
-        t_ao = graph_time(lambda: attention(qzo, sm, out=outo))
-        pb = prologue_bytes(wo.B, wo.H, wo.S, 128)
-        other_configs.append({"workload": name, "attention_ms": t_ao * 1e3,
-                              "attention_tflops": float(wo.attention_ops) / t_ao / 1e12,
-                              "attention_frac_of_peak": float(wo.attention_ops) / t_ao / 1e12 / p_att_other,
-                              "prologue_ms": t_po * 1e3, "prologue_gbs": pb / t_po / 1e9,
-                              "prologue_frac_of_hbm": pb / t_po / 1e9 / peaks["hbm_gbs"]})
-        del qo, ko, vo, qzo, outo
     if device_error() != 0:
         raise RuntimeError("device error word set during timing")
+    configs = config_rows(torch, peaks, scrub, sm) if (rank == 0 and not args.no_configs) else None
     short_calls = short_call_latency(torch, sageattn, sm) if rank == 0 else None
 
     # --- end to end through the C ABI with pinned host buffers: every step
@@ -419,9 +530,14 @@ def run_gpu(args):
     # head groups' copies overlap the other groups' kernels)
     from quantized_attention_fp64_gb300 import host_workspace_size, sageattn_host
 
-    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-    oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    ws_host = torch.empty(host_workspace_size(B, S, H, D), dtype=torch.uint8, device="cuda")
+    if strong:
+        qh, kh, vh = (t.contiguous().cpu().pin_memory() for t in (qb, kb, vb))
+        hb = h1 - h0
+    else:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        hb = H
+    oh = torch.empty(qh.shape, dtype=torch.bfloat16, pin_memory=True)
+    ws_host = torch.empty(host_workspace_size(B, S, hb, D), dtype=torch.uint8, device="cuda")
 
     def e2e_step():
         sageattn_host(qh, kh, vh, tensor_layout="NHD", sm_scale=sm, out=oh, workspace=ws_host)
@@ -431,50 +547,56 @@ def run_gpu(args):
     torch.cuda.synchronize()
     step()  # the device path's result (out last held a causal timing run)
     torch.cuda.synchronize()
-    if not torch.equal(oh, out.cpu()):
+    if not torch.equal(oh, (out_b if strong else out).cpu()):
         raise RuntimeError("host-buffer path disagrees with the device path")
+    barrier(world)
     ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ee0.record(stream)
     for _ in range(args.steps):
         e2e_step()
     ee1.record(stream)
     torch.cuda.synchronize()
+    barrier(world)
     t_e2e = max_over_ranks(ee0.elapsed_time(ee1) / 1e3 / args.steps, world)
     del ws_host
 
-    n_elem = B * S * H * D
+    n_elem = B * S * hb * D
     s_pad = -(-S // 128) * 128
     pro_bytes = prologue_bytes(B, H, S, D)
     # sage_quantize also writes the fp16 copies of the Q/K codes the tensor
     # cores read (sm_103a has no int8 MMA kind)
     pro_moved = pro_bytes + 4 * B * H * s_pad * D
     p_att, p16, p8 = attention_peak(peaks)
-    att_tflops = ops / t_att / 1e12
+    att_tflops = ops_total / t_att / 1e12
     line = {
         "metric": METRIC,
-        "value": world * ops / t_step / 1e12,
+        "value": job_ops / t_step / 1e12,
         "unit": "TOPS",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": t_step * 1e3,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if strong else "weak",
         "vs_baseline": None,
         "dtype": "int8 QK (exact on fp16 tensor cores), e4m3 PV, fp32 softmax",
         "data": "synthetic",
-        "config": bench_config(world),
+        "config": bench_config(world, strong),
         "roofline": {"kernel": "attention_tc", "bound": "tensor", "achieved": att_tflops, "peak": p_att,
                      "unit": "TFLOP/s", "frac": att_tflops / p_att, "traffic": attention_traffic(),
-                     "traffic_unit": "bytes per launch (DRAM read + write, one ncu capture)",
+                     "traffic_unit": "bytes per launch (DRAM read + write, one ncu capture of this source)",
                      "peak_note": f"harmonic mean of fp16 {p16:.1f} and e4m3 {p8:.1f} TFLOP/s "
                                   f"({peak_kind} bf16 burst: the kernel is timed alone; e4m3 = 2x nominal ratio)"},
-        "attention_kernel": {"ms": t_att * 1e3, "tflops": att_tflops, "frac_of_peak": att_tflops / p_att},
+        "attention_kernel": {"ms": t_att * 1e3, "tflops": att_tflops, "frac_of_peak": att_tflops / p_att,
+                             "cold_l2_ms": t_att_cold * 1e3,
+                             "cold_l2_frac_of_peak": ops_total / t_att_cold / 1e12 / p_att},
         "attention_kernel_causal": {"ms": t_att_causal * 1e3, "visible_ops": ops_causal,
                                     "tflops": ops_causal / t_att_causal / 1e12,
                                     "frac_of_peak": ops_causal / t_att_causal / 1e12 / p_att},
         "prologue": {"ms": t_pro * 1e3, "call": "sage_quantize", "algorithmic_bytes": pro_bytes,
                      "gbs": pro_bytes / t_pro / 1e9, "frac_of_hbm": pro_bytes / t_pro / 1e9 / peaks["hbm_gbs"],
+                     "cold_l2_ms": t_pro_cold * 1e3, "cold_l2_gbs": pro_bytes / t_pro_cold / 1e9,
+                     "cold_l2_frac_of_hbm": pro_bytes / t_pro_cold / 1e9 / peaks["hbm_gbs"],
                      "bytes_written_and_read": pro_moved, "gbs_moved": pro_moved / t_pro / 1e9,
                      "peak_gbs": peaks["hbm_gbs"], "bound": "hbm"},
         "head_dim_64": {"workload": "B1_H28_S16384_D64", "attention_ms": t_att64 * 1e3,
@@ -483,9 +605,9 @@ def run_gpu(args):
                         "prologue_ms": t_pro64 * 1e3,
                         "prologue_gbs": 9 * w64.B * w64.H * w64.S * 64 / t_pro64 / 1e9,
                         "prologue_frac_of_hbm": 9 * w64.B * w64.H * w64.S * 64 / t_pro64 / 1e9 / peaks["hbm_gbs"]},
-        "other_configs": other_configs,
+        "configs": configs,
         "short_calls": short_calls,
-        "e2e": {"value": world * ops / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": 3 * 2 * n_elem,
+        "e2e": {"value": job_ops / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": 3 * 2 * n_elem,
                 "d2h_bytes_per_step": 2 * n_elem, "ms_per_step": t_e2e * 1e3,
                 "call": "sage_sageattn_host (pinned host q, k, v, out; head groups' copies overlap the kernels)"},
         # per step: the prologue kernel and the attention kernel (plus one
@@ -497,8 +619,6 @@ def run_gpu(args):
         line["cpu_baseline"] = cpu_oracle_sample(rows=args.cpu_rows, heads=args.cpu_heads)
     if rank == 0:
         print(json.dumps(line))
-    from quantized_attention_fp64_gb300 import dist
-
     dist.teardown(world)
     return 0
 
@@ -513,6 +633,10 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=16384, help="query rows per head of the cpu_baseline sample")
     ap.add_argument("--cpu-heads", type=int, default=2, help="heads of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration table")
+    ap.add_argument("--strong", action="store_true",
+                    help="with N > 1: split the workload's heads over the ranks (strong scaling) instead of "
+                         "running one replica per rank")
     ap.add_argument("--profile", action="store_true", help="run one prologue + attention on --workload and exit")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--causal", action="store_true", help="with --profile: the attention call with the causal mask")
