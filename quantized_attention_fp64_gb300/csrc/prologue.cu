@@ -87,7 +87,7 @@ constexpr uint32_t kHstatBytes = 3 * kHeadDim * 4;  // key mean, V scales, their
 constexpr uint32_t kOffBar = kOffHstat + kStages * kHstatBytes;
 constexpr int kNumBars = 2 * kStages + 2 * kEvents;  // full, empty, event full, event empty
 constexpr uint32_t kOffMeta = kOffBar + kNumBars * 8;
-constexpr uint32_t kOffEvt = kOffMeta + kStages * 16;
+constexpr uint32_t kOffEvt = kOffMeta + kStages * 24;  // per stage: item (or head), head, group | phase << 32
 constexpr uint32_t kOffFinQ = kOffEvt + kEvents * 8;
 constexpr uint32_t kOffFlags = kOffFinQ + kFinCap * 8;  // abort flag, finish-queue tail, groups counted
 constexpr uint32_t kSmemBytes = kOffFlags + 16 + 1024;  // + alignment slack
@@ -435,7 +435,10 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return r;
 }
 
-// Exact path of four V codes (out of line: rare); low byte = channel 0.
+// Exact path of four V codes (out of line; with bf16 inputs, v / s_v =
+// 448 v / vmax falls exactly on an e4m3 rounding midpoint often enough that
+// some lane of a warp needs it for many tokens, but inlining it measured
+// slower); low byte = channel 0.
 __device__ __noinline__ uint32_t exact_v_quad(uint2 w, float4 s) {
   const uint32_t p01 = e4m3x2(__fdiv_rn(hi_bf16(w.x), s.y), __fdiv_rn(lo_bf16(w.x), s.x));
   const uint32_t p23 = e4m3x2(__fdiv_rn(hi_bf16(w.y), s.w), __fdiv_rn(lo_bf16(w.y), s.z));
@@ -737,7 +740,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     prologue_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params prm, int3 s_axis) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // aligned by pointer arithmetic on the shared array (an integer round trip
+  // would hide the address space and turn every tile read into a generic load)
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   // the statistics of the group a team is working on (either team can be)
   __shared__ double ks[kTeams][kChunks][kHeadDim];            // exact chunk sums
   __shared__ uint32_t vm[kTeams][kWarps][kHeadDim / 2];       // per-warp max |v| bits, channel pairs
@@ -753,7 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = tc::smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t* meta_item = reinterpret_cast<int64_t*>(smem + kOffMeta);             // [kStages]
-  int* meta_tensor = reinterpret_cast<int*>(smem + kOffMeta + kStages * 8);     // [kStages]
+  int64_t* meta_bh = reinterpret_cast<int64_t*>(smem + kOffMeta + kStages * 8); // [kStages]
+  // [kStages]: the tensor in the low 32 bits, the item's phase in bit 32, its
+  // group above (the producer decodes each item once: 64-bit division by the
+  // group count in every consumer thread cost several percent of the kernel)
+  int64_t* meta_tg = reinterpret_cast<int64_t*>(smem + kOffMeta + kStages * 16);
   volatile int64_t* evt_bh = reinterpret_cast<volatile int64_t*>(smem + kOffEvt);  // [kEvents]
   int64_t* fin_q = reinterpret_cast<int64_t*>(smem + kOffFinQ);                 // [kFinCap]
   const float* hstat = reinterpret_cast<const float*>(smem + kOffHstat);        // [kStages][256]
@@ -838,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto push_finish = [&](uint32_t st) {
         __threadfence_block();  // the queue entry after its tail
         meta_item[st] = fin_q[fin_head++ % kFinCap];
-        meta_tensor[st] = kFinish;
+        meta_tg[st] = kFinish;
         tc::mbar_arrive(cx.full(st));
         ++cnt;
       };
@@ -890,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (fins_waiting()) continue;
             if (!(ok = next_stage(st, ph))) break;
             meta_item[st] = -1;
-            meta_tensor[st] = kEnd;
+            meta_tg[st] = kEnd;
             tc::mbar_arrive(cx.full(st));
             break;
           }
@@ -931,7 +940,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = 0; n < nt && ok; ++n) {
           if (!(ok = next_stage(st, ph))) break;
           meta_item[st] = item;
-          meta_tensor[st] = tensors[n];
+          meta_bh[st] = it.bh;
+          meta_tg[st] = static_cast<int64_t>(tensors[n]) | (static_cast<int64_t>(it.phase) << 32) | (it.g << 33);
           const bool with_stats = it.phase == 1 && n == 0;  // the codes item's head statistics
           tc::mbar_arrive_expect_tx(cx.full(st), kTileBytes + (with_stats ? kHstatBytes : 0u));
           const CUtensorMap* tm = tensors[n] == kTensorQ ? &tm_q : (tensors[n] == kTensorK ? &tm_k : &tm_v);
@@ -994,7 +1004,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t st = cnt % kStages;
     if (!wait_bar(cx, cx.full(st), (cnt / kStages) & 1u)) break;
     const int64_t item = meta_item[st];
-    const int tensor = meta_tensor[st];
+    const int64_t tg = meta_tg[st];
+    const int tensor = static_cast<int>(tg & 0xFFFFFFFF);
     if (tensor == kEnd) {
       if (team == 1 && tt == 0) {
         // tell the counter warp that no report follows
@@ -1012,7 +1023,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       cnt += 1;
       continue;
     }
-    const Item it = decode_item(item, prm.NH, G, prm.lag);
+    Item it;
+    it.phase = static_cast<int>((tg >> 32) & 1);
+    it.bh = meta_bh[st];
+    it.g = tg >> 33;
     const uint32_t n_stages = it.phase == 0 ? (prm.smooth_k ? 3u : 2u) : 2u;
     // the two teams swap roles from one item of a kind to the next, so that
     // neither waits for the other's heavier tile (role 0: the Q tile of a
@@ -1161,7 +1175,7 @@ __global__ void __launch_bounds__(kShortThreads, 1)
     prologue_short_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const Params prm, int3 s_axis) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* smem = smem_raw + ((128u - (tc::smem_u32(smem_raw) & 127u)) & 127u);
   __shared__ double ks[kChunks][kHeadDim];       // exact chunk sums of this group
   __shared__ uint32_t vm[kWarps][kHeadDim / 2];  // per-warp max |v| bits, channel pairs
   __shared__ float xk_hi[kChunks][kHeadDim], xk_lo[kChunks][kHeadDim];  // second-half key sums
