@@ -300,6 +300,44 @@ SAGE_API int sage_sageattn_ex(const void* q_dev, const void* k_dev, const void* 
                               int out_dtype, float* lse_dev, void* workspace_dev, size_t workspace_bytes,
                               void* cuda_stream);
 
+/* Every argument of sage_sageattn_ex in one struct, with the same meaning,
+ * checks and errors (tensor_layout: "NHD" or "HND" with its terminating NUL;
+ * anything else is LAYOUT). lse_dev may be NULL. For callers whose
+ * per-argument marshalling costs more than the call itself (an interpreted
+ * binding): they keep one filled struct per signature (shapes, strides,
+ * dtypes, layout, flags) and change only the pointers, sm_scale and the
+ * stream between calls. The struct is read before the call returns and not
+ * kept. */
+typedef struct sage_sageattn_args {
+  const void* q_dev;
+  const void* k_dev;
+  const void* v_dev;
+  int64_t q_shape[4];
+  int64_t k_shape[4];
+  int64_t v_shape[4];
+  int64_t q_strides[4];
+  int64_t k_strides[4];
+  int64_t v_strides[4];
+  int64_t out_strides[4];
+  int32_t q_dtype;
+  int32_t k_dtype;
+  int32_t v_dtype;
+  int32_t out_dtype;
+  int32_t is_causal;
+  int32_t smooth_k;
+  float sm_scale;
+  char tensor_layout[4];
+  void* out_dev;
+  float* lse_dev;
+  void* workspace_dev;
+  size_t workspace_bytes;
+  void* cuda_stream;
+} sage_sageattn_args;
+
+/* sage_sageattn_ex on the arguments in *args. Errors: NULLPTR for a NULL
+ * args, otherwise those of sage_sageattn_ex. */
+SAGE_API int sage_sageattn_args_call(const sage_sageattn_args* args);
+
 /* sageattn on HOST buffers, end to end: q, k, v and out live in host memory
  * (page-locked memory lets the copies run asynchronously; pageable memory
  * works, with staged copies), each contiguous in tensor_layout ("NHD":

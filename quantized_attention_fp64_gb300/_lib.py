@@ -28,6 +28,17 @@ class Quantized(ctypes.Structure):
                 ("k16_dev", c_vp)]
 
 
+class SageattnArgs(ctypes.Structure):
+    """sage_sageattn_args"""
+    _fields_ = [("q_dev", c_vp), ("k_dev", c_vp), ("v_dev", c_vp), ("q_shape", I64x4), ("k_shape", I64x4),
+                ("v_shape", I64x4), ("q_strides", I64x4), ("k_strides", I64x4), ("v_strides", I64x4),
+                ("out_strides", I64x4), ("q_dtype", ctypes.c_int32), ("k_dtype", ctypes.c_int32),
+                ("v_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32), ("is_causal", ctypes.c_int32),
+                ("smooth_k", ctypes.c_int32), ("sm_scale", ctypes.c_float), ("tensor_layout", ctypes.c_char * 4),
+                ("out_dev", c_vp), ("lse_dev", c_vp), ("workspace_dev", c_vp), ("workspace_bytes", ctypes.c_size_t),
+                ("cuda_stream", c_vp)]
+
+
 _SIGNATURES = {
     "sage_bundle_size": (c_int, [c_i64, c_i64, c_i64, c_i64, c_size_p, c_vp, ctypes.POINTER(Quantized)]),
     "sage_quantize_scratch_size": (c_int, [c_i64, c_i64, c_i64, c_i64, c_size_p]),
@@ -51,6 +62,7 @@ _SIGNATURES = {
     "sage_sageattn_ex": (c_int, [c_vp, c_vp, c_vp, I64x4, I64x4, I64x4, I64x4, I64x4, I64x4, c_int, c_int, c_int,
                                  ctypes.c_char_p, c_int, ctypes.c_float, c_int, c_vp, I64x4, c_int, c_vp, c_vp,
                                  ctypes.c_size_t, c_vp]),
+    "sage_sageattn_args_call": (c_int, [ctypes.POINTER(SageattnArgs)]),
     "sage_host_workspace_size": (c_int, [c_i64, c_i64, c_i64, c_i64, c_int, c_size_p]),
     "sage_sageattn_host": (c_int, [c_vp, c_vp, c_vp, I64x4, c_int, ctypes.c_char_p, c_int, ctypes.c_float, c_int, c_vp,
                                    c_int, c_vp, ctypes.c_size_t, c_vp]),

@@ -49,6 +49,7 @@ constexpr int64_t kMaxElems = int64_t(1) << 44;
 int check_device(int* dev_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SAGE_ERR_CUDA;
+  if (bind_device_context(dev) != cudaSuccess) return SAGE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_arch_ok[dev] == 0) {
     int major = 0, minor = 0;
@@ -580,6 +581,16 @@ int sage_sageattn_ex(const void* q_dev, const void* k_dev, const void* v_dev, co
   return sageattn_impl(q_dev, k_dev, v_dev, q_shape, k_shape, v_shape, q_strides, k_strides, v_strides, q_dtype,
                        k_dtype, v_dtype, tensor_layout, is_causal != 0, sm_scale, lse_dev, smooth_k, out_dev,
                        out_strides, out_dtype, workspace_dev, workspace_bytes, cuda_stream);
+}
+
+int sage_sageattn_args_call(const sage_sageattn_args* a) {
+  if (a == nullptr) return SAGE_ERR_NULLPTR;
+  char layout[5] = {a->tensor_layout[0], a->tensor_layout[1], a->tensor_layout[2], a->tensor_layout[3], 0};
+  if (layout[3] != 0) return SAGE_ERR_LAYOUT;
+  return sageattn_impl(a->q_dev, a->k_dev, a->v_dev, a->q_shape, a->k_shape, a->v_shape, a->q_strides,
+                       a->k_strides, a->v_strides, a->q_dtype, a->k_dtype, a->v_dtype, layout, a->is_causal != 0,
+                       a->sm_scale, a->lse_dev, a->smooth_k, a->out_dev, a->out_strides, a->out_dtype,
+                       a->workspace_dev, a->workspace_bytes, a->cuda_stream);
 }
 
 int sage_device_error(void* cuda_stream, int* code) {

@@ -58,6 +58,9 @@ int sm_count_current();        // SMs of the current device (cached)
 // many bytes (the call costs microseconds, which short calls notice).
 cudaError_t set_smem_limit_once(const void* func, int bytes);
 size_t l2_bytes_current();     // L2 bytes of the current device (cached)
+// Makes the context of device `dev` (the current device) current in the
+// calling thread, once per thread and device.
+cudaError_t bind_device_context(int dev);
 
 // Launchers implemented by the kernel translation units. Each enqueues on
 // `stream` and returns the launch status (cudaGetLastError).

@@ -47,7 +47,7 @@ void* g_noalloc_ptr[kMaxDev] = {};
 // per device), or nullptr with *rc set.
 void* noalloc_scratch_ptr(int* rc) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev || bind_device_context(dev) != cudaSuccess) {
     *rc = SAGE_ERR_CUDA;
     return nullptr;
   }

@@ -61,6 +61,23 @@ cudaError_t set_smem_limit_once(const void* func, int bytes) {
   return e;
 }
 
+cudaError_t bind_device_context(int dev) {
+  // The driver calls the library makes before its first launch (tensor-map
+  // encoding) need the device's context current in the calling thread. A
+  // thread that has only run runtime calls that bind nothing (a framework's
+  // cached allocations, device queries) may not have it yet; cudaSetDevice
+  // initializes the device's primary context and makes it current (it is no
+  // stream operation, so it is also allowed while a stream is being
+  // captured). Once per thread and device.
+  thread_local uint64_t bound = 0;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t bit = uint64_t(1) << dev;
+  if (bound & bit) return cudaSuccess;
+  cudaError_t e = cudaSetDevice(dev);
+  if (e == cudaSuccess) bound |= bit;
+  return e;
+}
+
 int sm_count_current() {
   static int counts[64] = {};
   int dev = 0;

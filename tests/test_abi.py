@@ -234,3 +234,61 @@ def test_device_entries_without_a_device_return_an_error(lib):
     code = ctypes.c_int(0)
     assert lib.sage_selftest_wait_timeout(None) < 0
     assert lib.sage_device_error(None, ctypes.byref(code)) < 0
+
+
+def _args_struct(lse_ptr=0x60000, **over):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, shape=(1, 256, 2, 128), kshape=None, vshape=None,
+             strides=(256 * 2 * 128, 2 * 128, 128, 1), dt=0, kdt=0, vdt=0, layout=b"NHD", causal=1, sm=float("nan"),
+             smooth=1, out=0x40000, ostrides=None, odt=0, ws=0x50000, wsn=1 << 40)
+    a.update(over)
+    I = _lib.I64x4
+    s = _lib.SageattnArgs()
+    s.q_dev, s.k_dev, s.v_dev = a["q"], a["k"], a["v"]
+    s.q_shape, s.k_shape, s.v_shape = I(*a["shape"]), I(*(a["kshape"] or a["shape"])), I(*(a["vshape"] or a["shape"]))
+    s.q_strides = s.k_strides = s.v_strides = I(*a["strides"])
+    s.out_strides = I(*(a["ostrides"] or a["strides"]))
+    s.q_dtype, s.k_dtype, s.v_dtype, s.out_dtype = a["dt"], a["kdt"], a["vdt"], a["odt"]
+    s.is_causal, s.smooth_k, s.sm_scale = a["causal"], a["smooth"], a["sm"]
+    s.tensor_layout = a["layout"]
+    s.out_dev, s.lse_dev, s.workspace_dev, s.workspace_bytes = a["out"], lse_ptr, a["ws"], a["wsn"]
+    s.cuda_stream = None
+    return s
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dt=1), DTYPE), (dict(odt=1), DTYPE),
+    (dict(shape=(1, 256, 2, 96)), HEAD_DIM),
+    (dict(kshape=(1, 255, 2, 128)), SHAPE),
+    (dict(layout=b"BSH"), LAYOUT), (dict(layout=b"NHDX"), LAYOUT), (dict(layout=b"NH"), LAYOUT),
+    (dict(out=0x40004), ALIGN), (dict(lse_ptr=0x60002), ALIGN), (dict(q=0x10008), ALIGN),
+    (dict(ws=0), NULLPTR), (dict(out=0), NULLPTR), (dict(wsn=1000), WORKSPACE), (dict(sm=-1.0), ARG),
+    (dict(shape=(1, 2 ** 40, 2, 128), strides=(2 ** 48, 256, 128, 1)), TOO_LARGE),
+])
+def test_sageattn_args_call_checks_like_the_ex_entry(lib, over, code):
+    lse = over.pop("lse_ptr", 0x60000)
+    s = _args_struct(lse, **over)
+    assert lib.sage_sageattn_args_call(ctypes.byref(s)) == code
+    assert _call_sageattn_ex(lib, lse_ptr=lse, **over) == code
+    assert lib.sage_sageattn_args_call(None) == NULLPTR
+
+
+def test_sageattn_args_struct_matches_the_header(tmp_path):
+    # the binding's struct must have the C struct's size and field offsets
+    # (compiled here with the host compiler from include/sage.h)
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    fields = [f[0] for f in _lib.SageattnArgs._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "sage.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(sage_sageattn_args));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(sage_sageattn_args, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-I", str(_build.ROOT) + "/include", str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(_lib.SageattnArgs)
+    assert got[1:] == [getattr(_lib.SageattnArgs, f).offset for f in fields]

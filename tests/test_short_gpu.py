@@ -214,3 +214,88 @@ def test_sageattn_short_reuses_one_workspace(sage_lib):
         assert torch.equal(o, a)
     assert torch.equal(neg, sageattn(-q, k, v, sm_scale=SM))
     assert device_error() == 0
+
+
+def test_repeated_signature_takes_prepared_arguments(sage_lib):
+    """A call whose shapes, strides, dtypes, devices, layout and flags were seen
+    before runs from the kept arguments: it must give the first call's result
+    bit for bit, honour a new sm_scale and new inputs, keep layouts and flags
+    apart, and still reject tensors that differ from the kept signature."""
+    from quantized_attention_fp64_gb300 import SageError, api, sageattn_ex
+
+    calls = api._forget_calls()
+    w = custom(2, 4, 384, seed_index=3600, k_offset_std=1.5)
+    q, k, v = make_qkv(w, "cuda")
+    first = sageattn(q, k, v, sm_scale=SM)
+    assert len(calls) == 1
+    again = sageattn(q, k, v, sm_scale=SM)
+    other_scale = sageattn(q, k, v, sm_scale=0.5 * SM)
+    q2, k2, v2 = make_qkv(custom(2, 4, 384, seed_index=3601, k_offset_std=0.5), "cuda")
+    fresh = sageattn(q2, k2, v2, sm_scale=SM)
+    torch.cuda.synchronize()
+    assert torch.equal(first, again)
+    api._forget_calls()
+    assert torch.equal(other_scale, sageattn(q, k, v, sm_scale=0.5 * SM))
+    api._forget_calls()
+    assert torch.equal(fresh, sageattn(q2, k2, v2, sm_scale=SM))
+    # causal and the LSE through the ex entry point, twice each
+    c1 = sageattn_ex(q, k, v, is_causal=True, sm_scale=SM)
+    c2 = sageattn_ex(q, k, v, is_causal=True, sm_scale=SM)
+    o1, l1 = sageattn_ex(q, k, v, sm_scale=SM, return_lse=True)
+    o2, l2 = sageattn_ex(q, k, v, sm_scale=SM, return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2) and torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert not torch.equal(c1, first)
+    # the same sizes in HND (other strides) and a padded-stride view
+    qh, kh, vh = (t.transpose(1, 2).contiguous() for t in (q, k, v))
+    h1 = sageattn(qh, kh, vh, tensor_layout="HND", sm_scale=SM)
+    h2 = sageattn(qh, kh, vh, tensor_layout="HND", sm_scale=SM)
+    torch.cuda.synchronize()
+    assert torch.equal(h1, h2) and torch.equal(h1.transpose(1, 2), first)
+    # tensors that differ from a kept signature take the full checks
+    with pytest.raises((SageError, ValueError)):
+        sageattn(q, k.cpu(), v, sm_scale=SM)
+    with pytest.raises(SageError):
+        sageattn(q, k.to(torch.float16), v, sm_scale=SM)
+    with pytest.raises(SageError):
+        sageattn(q, k[:, :200], v[:, :200], sm_scale=SM)
+    assert device_error() == 0
+
+
+def test_two_threads_on_one_stream(sage_lib):
+    """Two threads calling sageattn at once on the same stream (the library
+    call releases the GIL, so their launches interleave): every result must
+    equal the one computed alone."""
+    import threading
+
+    inputs = [make_qkv(custom(1, 4, 256 + 128 * (i % 3), seed_index=3700 + i, k_offset_std=1.0), "cuda")
+              for i in range(6)]
+    torch.cuda.synchronize()
+    alone = []
+    for q, k, v in inputs:
+        alone.append(sageattn(q, k, v, sm_scale=SM))
+        torch.cuda.synchronize()
+    results = {}
+    errors = []
+
+    def worker(t):
+        try:
+            outs = []
+            for rep in range(40):
+                i = (t + 2 * rep) % len(inputs)
+                outs.append((i, sageattn(*inputs[i], sm_scale=SM)))
+            results[t] = outs
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=120)
+    torch.cuda.synchronize()
+    assert not errors and len(results) == 2
+    for outs in results.values():
+        for i, o in outs:
+            assert torch.equal(o, alone[i])
+    assert device_error() == 0
