@@ -53,9 +53,10 @@ struct Out {
 bool make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
                const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
 int sm_count_current();        // SMs of the current device (cached)
-// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes) on the
-// current device, skipped when it was already done there for at least that
-// many bytes (the call costs microseconds, which short calls notice).
+// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes) and the
+// largest shared-memory carve-out on the current device, skipped when it was
+// already done there for at least that many bytes (the calls cost
+// microseconds, which short calls notice).
 cudaError_t set_smem_limit_once(const void* func, int bytes);
 size_t l2_bytes_current();     // L2 bytes of the current device (cached)
 // Makes the context of device `dev` (the current device) current in the

@@ -1159,19 +1159,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // chain each warp runs stays short (short calls wait for it): team 0 takes
 // the V maxima, codes Q while the group results are exchanged, then codes V;
 // team 1 sums K, exchanges the results, finishes the head's statistics and
-// codes K. Each CTA stores its group's key sums and V maxima
-// into the shared memory of every CTA of the cluster; after one cluster
-// barrier all of them hold every group's results, so the prologue is a
-// single launch with no global counters and no scratch, and each input byte
-// is read once. The arithmetic is the persistent kernel's (the same per-warp
-// helpers; the same pairwise tree over the group sums, padded with +0.0 to a
-// power of two, where padding changes nothing), so the outputs are
-// identical.
+// codes K. Each CTA keeps its group's key sums and V maxima in its own
+// shared memory; after a cluster barrier every CTA reads all G of them over
+// distributed shared memory, and a last cluster barrier, waited on at exit,
+// keeps each CTA resident until the others have read it. So the prologue is
+// a single launch with no global counters and no scratch, and each input byte
+// is read once. The shared memory (about 110 KB) and the 64 registers a
+// thread leave room for two CTAs per SM, which lets every cluster of 8 CTAs
+// of a 16-head problem run at once (with one CTA per SM the GPU holds 15 of
+// them, and the 16th ran in a second wave). The arithmetic is the
+// persistent kernel's (the same per-warp helpers; the same pairwise tree
+// over the group sums, padded with +0.0 to a power of two, where padding
+// changes nothing), so the outputs are identical.
 constexpr int kShortMaxGroups = 8;                 // the portable cluster size
 constexpr int kShortThreads = kTeams * kTeamThreads;
 constexpr uint32_t kShortSmemBytes = 3 * kTileBytes + 128;  // Q, K, V tiles + alignment slack
 
-__global__ void __launch_bounds__(kShortThreads, 1)
+__global__ void __launch_bounds__(kShortThreads, 2)
     prologue_short_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const Params prm, int3 s_axis) {
   extern __shared__ uint8_t smem_raw[];
@@ -1181,8 +1185,8 @@ __global__ void __launch_bounds__(kShortThreads, 1)
   __shared__ float xk_hi[kChunks][kHeadDim], xk_lo[kChunks][kHeadDim];  // second-half key sums
   __shared__ uint32_t xk_bits[kChunks][32];      // second-half magnitude bounds per lane
   __shared__ float xa[kTeams * kWarps / 2][2];   // block amax exchange of each warp pair
-  __shared__ double g_sum[kShortMaxGroups][kHeadDim];    // every group's key sums (stored by the cluster)
-  __shared__ uint32_t g_max[kShortMaxGroups][kHeadDim];  // every group's max |v| bits
+  __shared__ double g_sum[kHeadDim];    // this group's key sums (read by the whole cluster)
+  __shared__ uint32_t g_max[kHeadDim];  // this group's max |v| bits
   __shared__ __align__(16) float h_mean[kHeadDim];
   __shared__ __align__(16) float h_vscale[kHeadDim];
   __shared__ __align__(16) float h_vrcp[kHeadDim];
@@ -1268,6 +1272,7 @@ __global__ void __launch_bounds__(kShortThreads, 1)
                                                                         &xa[pair][sub], &xa[pair][sub ^ 1], pair);
     if (sub == 0 && lane == 0) prm.out.q_scale[bh * nblk + s0c / kQKBlock] = s;
     tc::cluster_wait_acquire();
+    tc::cluster_arrive_relaxed();  // team 0 reads no other CTA's shared memory
     asm volatile("bar.sync 2, %0;" ::"n"(kShortThreads) : "memory");  // the V scales are in h_vscale
     // V codes, transposed (4-channel lanes)
     v_codes_rows(v_rows, nv, lane, *reinterpret_cast<const float4*>(h_vscale + 4 * lane),
@@ -1284,8 +1289,7 @@ __global__ void __launch_bounds__(kShortThreads, 1)
     const int c = tt - kTeamThreads;
     if (c < kHeadDim) {
       // the group's results: levels 1 and 2 of the pairwise tree over its 4
-      // chunk sums, and its max |v| per channel, stored into slot g of every
-      // CTA of the cluster (this one included)
+      // chunk sums, and its max |v| per channel, kept here for the cluster
       const double gs =
           prm.smooth_k ? __dadd_rn(__dadd_rn(ks[0][c], ks[1][c]), __dadd_rn(ks[2][c], ks[3][c])) : 0.0;
       uint32_t mb = 0u;
@@ -1294,26 +1298,30 @@ __global__ void __launch_bounds__(kShortThreads, 1)
         const uint32_t pr = vm[i][c >> 1];
         mb = max(mb, (c & 1) ? (pr >> 16) : (pr & 0xFFFFu));
       }
-      const uint32_t a_sum = tc::smem_u32(&g_sum[g][c]), a_max = tc::smem_u32(&g_max[g][c]);
-      for (int r = 0; r < G; ++r) {
-        tc::st_cluster_f64(tc::mapa_shared(a_sum, static_cast<uint32_t>(r)), gs);
-        tc::st_cluster_u32(tc::mapa_shared(a_max, static_cast<uint32_t>(r)), mb);
-      }
+      g_sum[c] = gs;
+      g_max[c] = mb;
     }
-    // every group's results are in every CTA's shared memory; after this
-    // barrier no CTA touches another's shared memory, so each may exit freely
+    // after this barrier every CTA's group results are visible to the cluster
     tc::cluster_arrive_release();
     tc::cluster_wait_acquire();
+    double lv[kShortMaxGroups];
+    float vmx = 0.0f;
+    if (c < kHeadDim) {
+      const uint32_t a_sum = tc::smem_u32(&g_sum[c]), a_max = tc::smem_u32(&g_max[c]);
+#pragma unroll
+      for (int r = 0; r < kShortMaxGroups; ++r) {
+        lv[r] = r < G ? tc::ld_cluster_f64(tc::mapa_shared(a_sum, static_cast<uint32_t>(r))) : 0.0;
+        if (r < G)
+          vmx = fmaxf(vmx, __uint_as_float(tc::ld_cluster_u32(tc::mapa_shared(a_max, static_cast<uint32_t>(r)))
+                                           << 16));
+      }
+    }
+    // this thread reads no other CTA's shared memory from here on (release:
+    // the loads above are complete before a CTA they read may exit)
+    tc::cluster_arrive_release();
     if (c < kHeadDim) {
       // the head's key mean and V scale of channel c (the same in every CTA):
       // the pairwise tree over the P = 2^ceil(log2 G) group sums
-      double lv[kShortMaxGroups];
-      float vmx = 0.0f;
-#pragma unroll
-      for (int r = 0; r < kShortMaxGroups; ++r) {
-        lv[r] = r < G ? g_sum[r][c] : 0.0;
-        if (r < G) vmx = fmaxf(vmx, __uint_as_float(g_max[r][c] << 16));
-      }
 #pragma unroll
       for (int w = 1; w < kShortMaxGroups; w *= 2) {
         if (w >= G) break;  // lv[0] already holds the tree of the first P leaves
@@ -1361,6 +1369,8 @@ __global__ void __launch_bounds__(kShortThreads, 1)
     drain.abort_flag = &no_abort;
     for (int n = 0; n < 3; ++n) wait_bar(drain, cx.full(n), 0);
   }
+  // the other CTAs of the cluster have read this one's group results
+  tc::cluster_wait_acquire();
 }
 
 struct ScratchLayout {

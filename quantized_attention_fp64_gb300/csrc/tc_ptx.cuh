@@ -164,6 +164,18 @@ __device__ __forceinline__ void st_cluster_f64(uint32_t addr, double v) {
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+// Loads from another CTA's shared memory (shared::cluster addresses from
+// mapa_shared), after a cluster barrier that made the values visible.
+__device__ __forceinline__ double ld_cluster_f64(uint32_t addr) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start before the previous kernel in its stream ends;

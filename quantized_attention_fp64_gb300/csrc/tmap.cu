@@ -57,6 +57,11 @@ cudaError_t set_smem_limit_once(const void* func, int bytes) {
   for (int i = 0; i < n_seen; ++i)
     if (seen[i].func == func && seen[i].dev == dev && seen[i].bytes >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  // the largest shared-memory share of the unified L1: the kernels stage
+  // their data in shared memory, and kernels that fit two CTAs per SM need
+  // the whole carve-out for it
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && n_seen < 128) seen[n_seen++] = Entry{func, dev, bytes};
   return e;
 }
