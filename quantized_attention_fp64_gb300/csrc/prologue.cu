@@ -45,8 +45,8 @@
 // (quantize_half_block). For e4m3, rounding is monotone, so when
 // q = fl(v*fl(1/s)) scaled by (1 - 2^-21) and by (1 + 2^-21) round to the same
 // code, fl(v/s) (within 2^-22 relative of q) does too; otherwise the exact
-// division decides (v_code_quad_fast, exact_v_quad). Q and V maxima are taken on the bf16 bit
-// patterns, whose magnitudes order as integers.
+// division decides, element by element (v_code_brackets, v_codes_exact). Q and V maxima are taken
+// on the bf16 bit patterns, whose magnitudes order as integers.
 #include <cuda_fp16.h>
 
 #include <cfloat>
@@ -435,30 +435,49 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return r;
 }
 
-// Exact path of four V codes (out of line; with bf16 inputs, v / s_v =
-// 448 v / vmax falls exactly on an e4m3 rounding midpoint often enough that
-// some lane of a warp needs it for many tokens, but inlining it measured
-// slower); low byte = channel 0.
-__device__ __noinline__ uint32_t exact_v_quad(uint2 w, float4 s) {
-  const uint32_t p01 = e4m3x2(__fdiv_rn(hi_bf16(w.x), s.y), __fdiv_rn(lo_bf16(w.x), s.x));
-  const uint32_t p23 = e4m3x2(__fdiv_rn(hi_bf16(w.y), s.w), __fdiv_rn(lo_bf16(w.y), s.z));
-  return p01 | (p23 << 16);
-}
-
 // Fast V codes of one token's 4 channels (4-channel lanes), low byte =
-// channel 0; returns false when the exact division must decide. Rounding to
-// e4m3 is monotone, and fl(v / s) lies within 2^-22 relative of
-// q = fl(v * fl(1/s)); so when q * (1 - 2^-21) and q * (1 + 2^-21) round to
-// the same code, that is the code of fl(v / s).
-__device__ __forceinline__ bool v_code_quad_fast(uint2 w, float2 r01, float2 r23, uint32_t& code) {
+// channel 0: the codes of q * (1 - 2^-21) in cd and of q * (1 + 2^-21) in
+// cu, q = fl(v * fl(1/s)). Rounding to e4m3 is monotone, and fl(v / s) lies
+// within 2^-22 relative of q; so where the two agree, that is the code of
+// fl(v / s), and where they differ the exact division must decide.
+__device__ __forceinline__ void v_code_brackets(uint2 w, float2 r01, float2 r23, uint32_t& cd, uint32_t& cu) {
   const float2 q01 = __fmul2_rn(bf2(w.x), r01), q23 = __fmul2_rn(bf2(w.y), r23);
   const float2 dn = make_float2(kDn, kDn), up = make_float2(kUp, kUp);
   const float2 d01 = __fmul2_rn(q01, dn), u01 = __fmul2_rn(q01, up);
   const float2 d23 = __fmul2_rn(q23, dn), u23 = __fmul2_rn(q23, up);
-  const uint32_t cd = e4m3x2(d01.y, d01.x) | (e4m3x2(d23.y, d23.x) << 16);
-  const uint32_t cu = e4m3x2(u01.y, u01.x) | (e4m3x2(u23.y, u23.x) << 16);
-  code = cd;
-  return cd == cu;
+  cd = e4m3x2(d01.y, d01.x) | (e4m3x2(d23.y, d23.x) << 16);
+  cu = e4m3x2(u01.y, u01.x) | (e4m3x2(u23.y, u23.x) << 16);
+}
+
+// One byte to global memory with the streaming hint.
+__device__ __forceinline__ void st_cs_u8(uint8_t* p, uint32_t v) {
+  asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Exact path of the V codes (out of line: rare per element, but with bf16
+// inputs v / s_v = 448 v / vmax falls exactly on an e4m3 rounding midpoint
+// for some channels, e.g. when s_v has few significant bits, so most warps
+// meet it somewhere). `redo` flags the tokens of this lane whose fast
+// brackets left a channel open (all: every kept channel is open, for scales
+// below FLT_MIN). For each, the brackets are recomputed and only the open
+// channels are divided exactly, each code stored again as one byte at
+// vt_lane[c * S_pad + t] over the fast one this thread stored before (same
+// thread, same address: the later store wins).
+__device__ __noinline__ void v_codes_exact(const uint8_t* rows, int lane, uint32_t redo, bool all, float2 r01,
+                                           float2 r23, float4 svs, uint32_t keep, uint8_t* vt_lane, int64_t S_pad) {
+  const float sc[4] = {svs.x, svs.y, svs.z, svs.w};
+  while (redo != 0u) {
+    const int t = __ffs(redo) - 1;
+    redo &= redo - 1u;
+    const uint2 w = tok4(rows, t, lane);
+    uint32_t cd, cu;
+    v_code_brackets(w, r01, r23, cd, cu);
+    const uint32_t open = (all ? 0xFFFFFFFFu : (cd ^ cu)) & keep;
+    const float v[4] = {lo_bf16(w.x), hi_bf16(w.x), lo_bf16(w.y), hi_bf16(w.y)};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if ((open >> (8 * c)) & 0xFFu) st_cs_u8(vt_lane + c * S_pad + t, e4m3x2(0.0f, __fdiv_rn(v[c], sc[c])) & 0xFFu);
+  }
 }
 
 // Exact fp64 sums of one 32-token key chunk, by the two warps of a pair
@@ -571,23 +590,18 @@ __device__ __forceinline__ void v_codes_rows(const uint8_t* rows, int nv, int la
   }
   const float2 r01 = make_float2(rv[0], rv[1]), r23 = make_float2(rv[2], rv[3]);
   uint32_t a[kHalfRows];  // a[t]: the 4 channels' codes of token t
-  uint32_t redo = 0u;     // bit t: token t needs the exact division
+  uint32_t redo = 0u;     // bit t: a channel of token t needs the exact division
 #pragma unroll
   for (int t = 0; t < kHalfRows; ++t) {
     a[t] = 0u;
     if (nv == kHalfRows || t < nv) {
-      uint32_t code;
-      if (!(v_code_quad_fast(tok4(rows, t, lane), r01, r23, code) && fast)) redo |= 1u << t;
-      a[t] = code & keep;
+      uint32_t cd, cu;
+      v_code_brackets(tok4(rows, t, lane), r01, r23, cd, cu);
+      if (!(cd == cu && fast)) redo |= 1u << t;
+      a[t] = cd & keep;
     }
   }
-  if (redo != 0u) {
-    // rare: tokens whose fast codes are not certain
-#pragma unroll
-    for (int t = 0; t < kHalfRows; ++t)
-      if ((redo >> t) & 1u) a[t] = exact_v_quad(tok4(rows, t, lane), svs) & keep;
-  }
-  release();
+  if (redo == 0u) release();
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     // 4x4 byte transposes: tokens 4j..4j+3 of channel 4*lane+c
@@ -599,6 +613,10 @@ __device__ __forceinline__ void v_codes_rows(const uint8_t* rows, int nv, int la
       cw[j] = __byte_perm(lo01, lo23, (c & 1) ? 0x7632 : 0x5410);
     }
     __stcs(reinterpret_cast<uint4*>(vt_bh + (4 * lane + c) * S_pad + s0), make_uint4(cw[0], cw[1], cw[2], cw[3]));
+  }
+  if (redo != 0u) {
+    v_codes_exact(rows, lane, redo, !fast, r01, r23, svs, keep, vt_bh + 4 * lane * S_pad + s0, S_pad);
+    release();
   }
 }
 
