@@ -165,14 +165,15 @@ SAGE_API int sage_host_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D
  * strides.
  * scratch_dev: at least sage_quantize_scratch_size bytes, 256-byte aligned;
  * its contents on entry do not matter and are clobbered.
- * Enqueued (D = 128): for S > 1024, a clear of the scratch header (work
- * counter, per-head flags) and one persistent kernel that computes the
- * statistics and Q codes, finishes each head (key mean, V scales), then
- * writes the K and V codes; for S <= 1024, one kernel launched in clusters of
- * ceil(S / 128) CTAs per head that exchange the head statistics through
- * distributed shared memory and does not touch the scratch (which must still
- * be passed, with the same size). Both give identical results.
- * (D = 64: three plain kernels, statistics, head finish and codes.)
+ * Enqueued: for S > 1024, a clear of the scratch header (work counter,
+ * per-head flags) and one persistent kernel that computes the statistics and
+ * Q codes, finishes each head (key mean, V scales), then writes the K and V
+ * codes; for S <= 1024, one kernel launched in clusters of ceil(S / 128) CTAs
+ * per head that exchange the head statistics through distributed shared
+ * memory and does not touch the scratch (which must still be passed, with the
+ * same size). Both give identical results. At D = 64 the same kernels run on
+ * head pairs (heads 2j and 2j + 1 as one 128-channel head; each keeps its own
+ * block scales and outputs).
  * Errors: NULLPTR, SHAPE, HEAD_DIM, ALIGN, WORKSPACE, TOO_LARGE, ARCH, CUDA. */
 SAGE_API int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k, const sage_bf16_tensor* v,
                   int64_t B, int64_t S, int64_t H, int64_t D, int smooth_k,
@@ -191,12 +192,12 @@ SAGE_API int sage_quantize(const sage_bf16_tensor* q, const sage_bf16_tensor* k,
  * Limit: where the prologue uses scratch, it must need at most 32 MiB of it:
  * sage_quantize_scratch_size(B, S, H, D) <= 32 MiB. That is about
  * B * H * (S_pad * 12 + 512) bytes at D = 128 (about 21 800 (head,
- * 128-token group) pairs) and B * H * S_pad * 24 bytes at D = 64 (about
- * 10 900 pairs), with S_pad = ceil(S / 128) * 128; larger problems are
- * rejected with SAGE_ERR_WORKSPACE and nothing is launched. At D = 128 with
- * S <= 1024 the prologue runs as one cluster kernel that uses no scratch, so
- * there the limit does not apply (only the library's general size limits,
- * SAGE_ERR_TOO_LARGE, as for sage_quantize).
+ * 128-token group) pairs) and B * ceil(H / 2) * (S_pad * 12 + 1536) bytes at
+ * D = 64 (about 43 600 pairs), with S_pad = ceil(S / 128) * 128; larger
+ * problems are rejected with SAGE_ERR_WORKSPACE and nothing is launched.
+ * With S <= 1024 the prologue runs as one cluster kernel that uses no
+ * scratch, so there the limit does not apply (only the library's general
+ * size limits, SAGE_ERR_TOO_LARGE, as for sage_quantize).
  * The first call on each device looks up the array's device address with
  * cudaGetSymbolAddress; make that first call before any stream capture.
  * All calls share the array and it keeps the last call's contents; each call

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "lib", "libsage.so")
-SOURCES = ["api.cu", "prologue.cu", "prologue64.cu", "attention_simt.cu", "attention_tc.cu", "lse_term.cu",
+SOURCES = ["api.cu", "prologue.cu", "attention_simt.cu", "attention_tc.cu", "lse_term.cu",
            "quantize_noalloc.cu", "tmap.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".cuh", ".h"))] + [
     os.path.join(ROOT, "include", "sage.h")]

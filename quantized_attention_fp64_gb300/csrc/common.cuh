@@ -67,20 +67,16 @@ cudaError_t bind_device_context(int dev);
 // `stream` and returns the launch status (cudaGetLastError).
 // write_int8: also store the int8 Q/K codes (the fp16 copies, V codes and
 // all scales are always written). dev_err: the device error word.
-// D: the head dimension (128 or 64).
+// D: the head dimension (128 or 64; 64 runs the same kernels on head pairs).
 cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, int64_t B, int64_t S,
                             int64_t H, int64_t D, bool smooth_k, const Bundle& out, void* scratch, bool write_int8,
                             int* dev_err, cudaStream_t stream);
-// The head-dimension-64 prologue (three plain kernels) and its scratch.
-cudaError_t launch_prologue64(const Bf16In& q, const Bf16In& k, const Bf16In& v, int64_t B, int64_t S, int64_t H,
-                              bool smooth_k, const Bundle& out, void* scratch, bool write_int8, cudaStream_t stream);
-size_t prologue64_scratch_bytes(int64_t B, int64_t S, int64_t H);
 // Device address of the current device's error word (set up on first use),
 // or nullptr if the runtime call fails.
 int* device_error_ptr();
 size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H, int64_t D);
 // Whether launch_prologue touches its scratch for this shape (the cluster
-// kernel of short sequences at D = 128 does not).
+// kernel of short sequences does not).
 bool prologue_uses_scratch(int64_t S, int64_t D);
 // The size limits every entry point applies: SAGE_OK or a negative SAGE_ERR_*
 // code (SHAPE, HEAD_DIM, TOO_LARGE).

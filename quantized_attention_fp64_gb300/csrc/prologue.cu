@@ -93,7 +93,8 @@ constexpr uint32_t kOffFlags = kOffFinQ + kFinCap * 8;  // abort flag, finish-qu
 constexpr uint32_t kSmemBytes = kOffFlags + 16 + 1024;  // + alignment slack
 
 struct Params {
-  int64_t S, S_pad, H, NH, G, lag, total;
+  int64_t S, S_pad, H, NH, G, lag, total;  // H, NH: (virtual) heads per batch and in all
+  int64_t Hr;  // head-pair mode: the real head count per batch
   int smooth_k, write_int8;
   Bundle out;
   unsigned* next_item;
@@ -102,8 +103,62 @@ struct Params {
   double* ksum;     // [NH][G][128]
   float* vmax;      // [NH][G][128]
   float* vrcp;      // [NH][128]: fl(1/s_v) of each finished head (0 for s_v < FLT_MIN)
+  float* hstat_v;   // head-pair mode: [NH][256] key mean and V scales of each finished virtual head
   int* dev_err;
 };
+
+// Head-pair mode (head dimension 64): virtual head bh = b * H + hp holds the
+// real heads 2hp and 2hp + 1 of batch b side by side, as channels 0-63 and
+// 64-127 of a 128-channel row, so the kernels below run unchanged on them;
+// only the per-block INT8 scales are per real head, and the outputs go to
+// the real heads' places in a head-dimension-64 bundle. out_head returns the
+// bundle head index (b * Hr + h) of half hf of bh, or -1 for the missing
+// second head of an odd head count (its input rows read as zeros).
+template <bool kPair>
+__device__ __forceinline__ int64_t out_head(const Params& prm, int64_t bh, int hf) {
+  if (!kPair) return bh;
+  const int64_t b = bh / prm.H, h = 2 * (bh % prm.H) + hf;
+  return h < prm.Hr ? b * prm.Hr + h : -1;
+}
+template <bool kPair>
+constexpr int kOutDim = kPair ? kHeadDim / 2 : kHeadDim;
+
+// The lane's output positions for quantize_half_block (8-channel lanes) at
+// token s0 of virtual head bh: c16 in the fp16 code copies and c8 in the
+// int8 codes (null unless `codes`); both null for a missing head. Returns
+// the lane's bundle head index.
+template <bool kPair>
+__device__ __forceinline__ int64_t lane_codes(const Params& prm, int8_t* codes, uint16_t* f16, int64_t bh,
+                                              int64_t s0, int lane, int8_t*& c8, uint16_t*& c16) {
+  const int64_t head = out_head<kPair>(prm, bh, kPair ? (lane >> 3) & 1 : 0);
+  if (head < 0) {
+    c8 = nullptr;
+    c16 = nullptr;
+    return head;
+  }
+  const int64_t off = (head * prm.S_pad + s0) * kOutDim<kPair> + 8 * (lane & (kPair ? 7 : 15));
+  c8 = codes ? codes + off : nullptr;
+  c16 = f16 + off;
+  return head;
+}
+
+// The scale of a 32-token block: lane 0 (and lane 8 with kPair) of the
+// block's first warp stores it for its head.
+template <bool kPair>
+__device__ __forceinline__ void store_block_scale(float* scales, int64_t head, int64_t nblk, int64_t blk, float s,
+                                                  int lane, int sub) {
+  if (sub == 0 && (kPair ? (lane & 23) == 0 : lane == 0) && head >= 0) scales[head * nblk + blk] = s;
+}
+
+// The lane's V-code position (4-channel lanes: channels 4*lane .. +3,
+// transposed rows S_pad apart) at token s0 of virtual head bh, or null for
+// a missing head.
+template <bool kPair>
+__device__ __forceinline__ uint8_t* lane_vt(const Params& prm, int64_t bh, int64_t s0, int lane) {
+  const int64_t head = out_head<kPair>(prm, bh, kPair ? lane >> 4 : 0);
+  if (head < 0) return nullptr;
+  return prm.out.vt_codes + (head * kOutDim<kPair> + ((4 * lane) & (kOutDim<kPair> - 1))) * prm.S_pad + s0;
+}
 
 struct Item {
   int phase;  // 0 stats, 1 codes
@@ -167,15 +222,21 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+// Maxima over the warp; with kPair over the 16 lanes that share bit 3 of the
+// lane index (with 8-channel lanes: the 64 channels of one head of a pair).
+template <bool kPair = false>
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = 16; o > 0; o >>= 1)
+    if (!(kPair && o == 8)) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
+template <bool kPair = false>
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = 16; o > 0; o >>= 1)
+    if (!(kPair && o == 8)) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
@@ -207,19 +268,23 @@ __device__ __noinline__ uint32_t exact_code_bits(float x, float s) {
 // channels as pairs). rows: the warp's 16 rows of a shared tile, read with
 // 8-channel lanes; nvalid: how many of them are below S (kFull: all 16). The
 // block's amax is the max of both halves: each warp posts its own in
-// x_mine and reads the other's from x_other after the pair barrier. Writes
-// rows s0 .. s0+15 of f16_bh ([S_pad][128], the codes as fp16 values) and,
-// when codes_bh is not null, of codes_bh ([S_pad][128] int8), with streaming
-// stores; rows at or past nvalid get zero codes. Returns the scale.
+// x_mine and reads the other's from x_other after the pair barrier. With
+// kPair the 128 channels are two heads of 64 (lanes with bit 3 clear and
+// set), each with its own amax, posted in x_mine[0] and x_mine[1]. c16 (and
+// c8, when not null) point at the lane's 8 channels of the warp's first row
+// in the fp16 code copies (and the int8 codes), rows `row_elems` apart; the
+// codes of rows s0 .. s0+15 go there with streaming stores, zero for rows at
+// or past nvalid; a null c16 (the missing head of an odd pair) stores
+// nothing. Returns the scale of the lane's head.
 //
 // Fast path for the codes (two-element packed arithmetic): t = fl(x*r + M)
 // with r = fl(1/s) and M = 1.5*2^23 is M + rint_even(x*r) (the spacing of
 // floats near M is 1); c = t - M exactly; g = fl(c - x*r). x*r is within
 // 2^-17 of x/s, and so is fl(x/s) (|x/s| <= 127.5), so when |g| < 1/2 - 2^-15
 // the code c is rint_even(fl(x/s)); otherwise the exact division decides.
-template <bool kMu, bool kFull>
+template <bool kMu, bool kFull, bool kPair = false>
 __device__ __forceinline__ float quantize_half_block(const uint8_t* rows, const float2 (&nmu)[4], int nvalid,
-                                                     int8_t* codes_bh, uint16_t* f16_bh, int64_t s0, int lane,
+                                                     int8_t* c8, uint16_t* c16, int row_elems, int lane,
                                                      volatile float* x_mine, volatile float* x_other, int pair) {
   const int half = lane >> 4;
   float a;
@@ -236,7 +301,7 @@ __device__ __forceinline__ float quantize_half_block(const uint8_t* rows, const 
       }
     }
     const uint32_t m = __vmaxu2(m0, m1);
-    a = __uint_as_float(warp_max_u32(max(m & 0xFFFFu, m >> 16)) << 16);
+    a = __uint_as_float(warp_max_u32<kPair>(max(m & 0xFFFFu, m >> 16)) << 16);
   } else {
     float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
@@ -252,24 +317,26 @@ __device__ __forceinline__ float quantize_half_block(const uint8_t* rows, const 
         a1 = max3(a1, fabsf(k3.x), fabsf(k3.y));
       }
     }
-    a = warp_max(fmaxf(a0, a1));
+    a = warp_max<kPair>(fmaxf(a0, a1));
   }
-  if (lane == 0) *x_mine = a;
+  const int hf = kPair ? (lane >> 3) & 1 : 0;
+  if (kPair ? (lane & 23) == 0 : lane == 0) x_mine[hf] = a;  // lanes 0 and 8 with kPair
   pair_bar(pair);
-  a = fmaxf(a, *x_other);
+  a = fmaxf(a, x_other[hf]);
   const float s = __fdiv_rn(a, kInt8Max);
   const bool fast = s >= FLT_MIN;
   const float r = fast ? __frcp_rn(s) : 0.0f;
   const float2 r2 = make_float2(r, r), nr2 = make_float2(-r, -r);
   const float2 m2 = make_float2(kMagic, kMagic), nm2 = make_float2(-kMagic, -kMagic);
-  uint2* out8 = codes_bh ? reinterpret_cast<uint2*>(codes_bh + s0 * kHeadDim) + (lane & 15) : nullptr;
-  uint4* out16 = reinterpret_cast<uint4*>(f16_bh + s0 * kHeadDim) + (lane & 15);
+  uint2* out8 = c16 != nullptr ? reinterpret_cast<uint2*>(c8) : nullptr;
+  uint4* out16 = reinterpret_cast<uint4*>(c16);
+  const int rs = row_elems / 8;  // row stride in 8-element units
   uint32_t redo = 0u;  // bit i: row 2i + half needs the exact division
 #pragma unroll
   for (int i = 0; i < kHalfRows / 2; ++i) {
     const int t = 2 * i + half;
-    uint2 c8 = make_uint2(0u, 0u);
-    uint4 c16 = make_uint4(0u, 0u, 0u, 0u);
+    uint2 c8v = make_uint2(0u, 0u);
+    uint4 c16v = make_uint4(0u, 0u, 0u, 0u);
     if ((kFull || t < nvalid) && a > 0.0f) {
       const uint4 w = tok8(rows, t, lane);
       float2 x[4] = {bf2(w.x), bf2(w.y), bf2(w.z), bf2(w.w)};
@@ -287,17 +354,17 @@ __device__ __forceinline__ float quantize_half_block(const uint8_t* rows, const 
         g = max3(g, fabsf(gk.x), fabsf(gk.y));
       }
       if (!(fast && g < kHalfGuard)) redo |= 1u << i;
-      c8 = make_uint2(pack_low_bytes(__float_as_uint(tt[0].x), __float_as_uint(tt[0].y), __float_as_uint(tt[1].x),
-                                     __float_as_uint(tt[1].y)),
-                      pack_low_bytes(__float_as_uint(tt[2].x), __float_as_uint(tt[2].y), __float_as_uint(tt[3].x),
-                                     __float_as_uint(tt[3].y)));
-      c16 = make_uint4(f16x2(cc[0].x, cc[0].y), f16x2(cc[1].x, cc[1].y), f16x2(cc[2].x, cc[2].y),
-                       f16x2(cc[3].x, cc[3].y));
+      c8v = make_uint2(pack_low_bytes(__float_as_uint(tt[0].x), __float_as_uint(tt[0].y), __float_as_uint(tt[1].x),
+                                      __float_as_uint(tt[1].y)),
+                       pack_low_bytes(__float_as_uint(tt[2].x), __float_as_uint(tt[2].y), __float_as_uint(tt[3].x),
+                                      __float_as_uint(tt[3].y)));
+      c16v = make_uint4(f16x2(cc[0].x, cc[0].y), f16x2(cc[1].x, cc[1].y), f16x2(cc[2].x, cc[2].y),
+                        f16x2(cc[3].x, cc[3].y));
     }
-    if (out8) __stcs(out8 + t * (kHeadDim / 8), c8);
-    __stcs(out16 + t * (kHeadDim / 8), c16);
+    if (out8) __stcs(out8 + t * rs, c8v);
+    if (out16) __stcs(out16 + t * rs, c16v);
   }
-  if (redo != 0u) {
+  if (redo != 0u && out16) {
     // rare: rows where a fast code could be off by one are recomputed by the
     // exact division and stored again (same thread, same address: the later
     // store wins)
@@ -319,9 +386,8 @@ __device__ __forceinline__ float quantize_half_block(const uint8_t* rows, const 
         cf[2 * k + 1] = __fsub_rn(__uint_as_float(b[2 * k + 1]), kMagic);
       }
       if (out8)
-        __stcs(out8 + t * (kHeadDim / 8),
-               make_uint2(pack_low_bytes(b[0], b[1], b[2], b[3]), pack_low_bytes(b[4], b[5], b[6], b[7])));
-      __stcs(out16 + t * (kHeadDim / 8),
+        __stcs(out8 + t * rs, make_uint2(pack_low_bytes(b[0], b[1], b[2], b[3]), pack_low_bytes(b[4], b[5], b[6], b[7])));
+      __stcs(out16 + t * rs,
              make_uint4(f16x2(cf[0], cf[1]), f16x2(cf[2], cf[3]), f16x2(cf[4], cf[5]), f16x2(cf[6], cf[7])));
     }
   }
@@ -573,12 +639,12 @@ __device__ __forceinline__ void v_max_rows(const uint8_t* vr, int nv, int lane, 
 }
 
 // e4m3 codes of one warp's 16 V rows (4-channel lanes: channels 4*lane ..
-// +4, scales svs), written transposed: 16 tokens of channel 4*lane+c at
-// vt_bh[(4*lane+c) * S_pad + s0]. Rows at or past nv get code 0. `release`
-// runs once the warp has stopped reading its rows.
+// +4, scales svs), written transposed: the 16 tokens of the lane's channel c
+// at vt_lane[c * S_pad] (nothing when vt_lane is null). Rows at or past nv
+// get code 0. `release` runs once the warp has stopped reading its rows.
 template <typename Release>
 __device__ __forceinline__ void v_codes_rows(const uint8_t* rows, int nv, int lane, float4 svs, float4 rvs,
-                                             uint8_t* vt_bh, int64_t S_pad, int64_t s0, Release release) {
+                                             uint8_t* vt_lane, int64_t S_pad, Release release) {
   const float sc[4] = {svs.x, svs.y, svs.z, svs.w};
   const float rv[4] = {rvs.x, rvs.y, rvs.z, rvs.w};  // fl(1/s) for s >= FLT_MIN, else 0
   uint32_t keep = 0u;
@@ -612,10 +678,10 @@ __device__ __forceinline__ void v_codes_rows(const uint8_t* rows, int nv, int la
       const uint32_t lo23 = __byte_perm(a[4 * j + 2], a[4 * j + 3], (c & 2) ? 0x7362 : 0x5140);
       cw[j] = __byte_perm(lo01, lo23, (c & 1) ? 0x7632 : 0x5410);
     }
-    __stcs(reinterpret_cast<uint4*>(vt_bh + (4 * lane + c) * S_pad + s0), make_uint4(cw[0], cw[1], cw[2], cw[3]));
+    if (vt_lane) __stcs(reinterpret_cast<uint4*>(vt_lane + c * S_pad), make_uint4(cw[0], cw[1], cw[2], cw[3]));
   }
   if (redo != 0u) {
-    v_codes_exact(rows, lane, redo, !fast, r01, r23, svs, keep, vt_bh + 4 * lane * S_pad + s0, S_pad);
+    if (vt_lane) v_codes_exact(rows, lane, redo, !fast, r01, r23, svs, keep, vt_lane, S_pad);
     release();
   }
 }
@@ -717,6 +783,9 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint32_t bar, uint32_t p
 // V codes multiply by, computed once here instead of once per item and warp);
 // then the head is published as ready. Every group of the head has
 // been counted (by the producer of this CTA, which saw the count complete).
+// With kPair the mean and scales go to the two real heads' places and, for
+// the codes items, to the virtual head's row of hstat_v.
+template <bool kPair>
 __device__ __forceinline__ void finish_head(const Params& prm, int64_t bh, int tt, double* fin_right,
                                             float* fin_vmax) {
   const int64_t G = prm.G;
@@ -740,9 +809,16 @@ __device__ __forceinline__ void finish_head(const Params& prm, int64_t bh, int t
       const double total = P > 1 ? __dadd_rn(t, fin_right[c]) : t;
       mu = __double2float_rn(__ddiv_rn(total, static_cast<double>(prm.S)));
     }
-    prm.out.k_mean[bh * kHeadDim + c] = mu;
     const float vs = __fdiv_rn(fmaxf(vmx, fin_vmax[c]), kE4M3Max);
-    prm.out.v_scale[bh * kHeadDim + c] = vs;
+    const int64_t head = out_head<kPair>(prm, bh, c / kOutDim<kPair>);
+    if (head >= 0) {
+      prm.out.k_mean[head * kOutDim<kPair> + (c & (kOutDim<kPair> - 1))] = mu;
+      prm.out.v_scale[head * kOutDim<kPair> + (c & (kOutDim<kPair> - 1))] = vs;
+    }
+    if (kPair) {
+      prm.hstat_v[bh * 2 * kHeadDim + c] = mu;
+      prm.hstat_v[bh * 2 * kHeadDim + kHeadDim + c] = vs;
+    }
     prm.vrcp[bh * kHeadDim + c] = vs >= FLT_MIN ? __frcp_rn(vs) : 0.0f;
   }
   team_bar(1);
@@ -754,6 +830,7 @@ __device__ __forceinline__ void finish_head(const Params& prm, int64_t bh, int t
   }
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     prologue_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params prm, int3 s_axis) {
@@ -766,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t vm[kTeams][kWarps][kHeadDim / 2];       // per-warp max |v| bits, channel pairs
   __shared__ float xk_hi[kTeams][kChunks][kHeadDim], xk_lo[kTeams][kChunks][kHeadDim];  // second-half key sums
   __shared__ uint32_t xk_bits[kTeams][kChunks][32];           // second-half magnitude bounds per lane
-  __shared__ float xa[2][kTeams * kWarps / 2][2];     // amax of each half block, two parities
+  __shared__ float xa[2][kTeams * kWarps / 2][2][2];  // amax of each half block (per head of a pair), two parities
   __shared__ float fin_vmax[kHeadDim];
   __shared__ double fin_right[kHeadDim];
   // the next kernel of the stream (the attention kernel, launched as a
@@ -953,7 +1030,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tensors[nt++] = kTensorK;
           tensors[nt++] = kTensorV;
         }
-        const int32_t h = static_cast<int32_t>(it.bh % prm.H), b = static_cast<int32_t>(it.bh / prm.H);
+        // the head coordinate: of the real head pair 2hp, 2hp + 1 in head-pair mode
+        const int32_t h = static_cast<int32_t>((kPair ? 2 : 1) * (it.bh % prm.H)), b = static_cast<int32_t>(it.bh / prm.H);
         const int32_t s0 = static_cast<int32_t>(it.g * kItemTokens);
         for (int n = 0; n < nt && ok; ++n) {
           if (!(ok = next_stage(st, ph))) break;
@@ -972,8 +1050,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tma_load_4d_hint(sbase + st * kTileBytes, tm, 0, h, s0, b, cx.full(st), pol);
           if (with_stats) {
             const uint32_t hs = sbase + kOffHstat + st * kHstatBytes;
-            tc::bulk_load(hs, prm.out.k_mean + it.bh * kHeadDim, kHeadDim * 4, cx.full(st));
-            tc::bulk_load(hs + kHeadDim * 4, prm.out.v_scale + it.bh * kHeadDim, kHeadDim * 4, cx.full(st));
+            const float* km = kPair ? prm.hstat_v + it.bh * 2 * kHeadDim : prm.out.k_mean + it.bh * kHeadDim;
+            const float* vsc = kPair ? prm.hstat_v + it.bh * 2 * kHeadDim + kHeadDim : prm.out.v_scale + it.bh * kHeadDim;
+            tc::bulk_load(hs, km, kHeadDim * 4, cx.full(st));
+            tc::bulk_load(hs + kHeadDim * 4, vsc, kHeadDim * 4, cx.full(st));
             tc::bulk_load(hs + 2 * kHeadDim * 4, prm.vrcp + it.bh * kHeadDim, kHeadDim * 4, cx.full(st));
           }
           pending[st] = static_cast<int>(ph);
@@ -1037,7 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tensor == kFinish) {
       tc::mbar_arrive(cx.empty(st));  // the marker carries no data
-      if (team == 1) finish_head(prm, item, tt, fin_right, fin_vmax);
+      if (team == 1) finish_head<kPair>(prm, item, tt, fin_right, fin_vmax);
       cnt += 1;
       continue;
     }
@@ -1056,21 +1136,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t s0c = it.g * kItemTokens + chunk * kQKBlock;  // first token of the chunk
     const int64_t s0 = s0c + sub * kHalfRows;                    // first token of this warp
     const int nv = valid_rows(S, s0, kHalfRows);  // this warp's rows below S (every row is below S_pad)
-    volatile float* xm = &xa[xpar][pair][sub];
-    volatile float* xo = &xa[xpar][pair][sub ^ 1];
+    volatile float* xm = &xa[xpar][pair][sub][0];
+    volatile float* xo = &xa[xpar][pair][sub ^ 1][0];
     bool ok = true;
 
     if (it.phase == 0 && role == 0) {
       // Q codes and scale
       const float2 nz[4] = {};
-      int8_t* qc = prm.write_int8 ? prm.out.q_codes + bh * S_pad * kHeadDim : nullptr;
-      uint16_t* q16 = prm.out.q16 + bh * S_pad * kHeadDim;
+      int8_t* qc;
+      uint16_t* q16;
+      const int64_t qh = lane_codes<kPair>(prm, prm.write_int8 ? prm.out.q_codes : nullptr, prm.out.q16, bh, s0, lane,
+                                           qc, q16);
       const uint8_t* rows = stage_rows(cnt);
-      const float s = nv == kHalfRows
-                          ? quantize_half_block<false, true>(rows, nz, kHalfRows, qc, q16, s0, lane, xm, xo, pair)
-                          : quantize_half_block<false, false>(rows, nz, nv, qc, q16, s0, lane, xm, xo, pair);
+      const float s = nv == kHalfRows ? quantize_half_block<false, true, kPair>(rows, nz, kHalfRows, qc, q16,
+                                                                                  kOutDim<kPair>, lane, xm, xo, pair)
+                                      : quantize_half_block<false, false, kPair>(rows, nz, nv, qc, q16,
+                                                                                   kOutDim<kPair>, lane, xm, xo, pair);
       xpar ^= 1;
-      if (sub == 0 && lane == 0) prm.out.q_scale[bh * nblk + s0c / kQKBlock] = s;
+      store_block_scale<kPair>(prm.out.q_scale, qh, nblk, s0c / kQKBlock, s, lane, sub);
       tc::mbar_arrive(cx.empty(st));
       for (uint32_t c = 1; c < n_stages && ok; ++c) ok = pass(cnt + c);
       if (!ok) break;
@@ -1137,14 +1220,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t c2 = cnt + 1;
       if (!wait_bar(cx, cx.full(c2 % kStages), (c2 / kStages) & 1u)) break;
       const uint32_t v_stage = c2 % kStages;
-      v_codes_rows(stage_rows(c2), nv, lane, svs, rvs, prm.out.vt_codes + bh * kHeadDim * S_pad, S_pad, s0,
+      v_codes_rows(stage_rows(c2), nv, lane, svs, rvs, lane_vt<kPair>(prm, bh, s0, lane), S_pad,
                    [&]() { tc::mbar_arrive(cx.empty(v_stage)); });
     } else {
       // codes item, team 1: K codes of k - mean; the key mean comes with the
       // K tile
-      int8_t* kc = prm.write_int8 ? prm.out.k_codes + bh * S_pad * kHeadDim : nullptr;
-      uint16_t* k16 = prm.out.k16 + bh * S_pad * kHeadDim;
+      int8_t* kc;
+      uint16_t* k16;
+      const int64_t kh = lane_codes<kPair>(prm, prm.write_int8 ? prm.out.k_codes : nullptr, prm.out.k16, bh, s0, lane,
+                                           kc, k16);
       const uint8_t* rows = stage_rows(cnt);
+      constexpr int od = kOutDim<kPair>;
       float skv;
       if (prm.smooth_k) {
         const float4* mp = reinterpret_cast<const float4*>(hstat + st * (kHstatBytes / 4) + 8 * (lane & 15));
@@ -1152,16 +1238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 nmu[4] = {make_float2(-ma.x, -ma.y), make_float2(-ma.z, -ma.w), make_float2(-mb.x, -mb.y),
                                make_float2(-mb.z, -mb.w)};
         skv = nv == kHalfRows
-                  ? quantize_half_block<true, true>(rows, nmu, kHalfRows, kc, k16, s0, lane, xm, xo, pair)
-                  : quantize_half_block<true, false>(rows, nmu, nv, kc, k16, s0, lane, xm, xo, pair);
+                  ? quantize_half_block<true, true, kPair>(rows, nmu, kHalfRows, kc, k16, od, lane, xm, xo, pair)
+                  : quantize_half_block<true, false, kPair>(rows, nmu, nv, kc, k16, od, lane, xm, xo, pair);
       } else {
         const float2 nz[4] = {};
         skv = nv == kHalfRows
-                  ? quantize_half_block<false, true>(rows, nz, kHalfRows, kc, k16, s0, lane, xm, xo, pair)
-                  : quantize_half_block<false, false>(rows, nz, nv, kc, k16, s0, lane, xm, xo, pair);
+                  ? quantize_half_block<false, true, kPair>(rows, nz, kHalfRows, kc, k16, od, lane, xm, xo, pair)
+                  : quantize_half_block<false, false, kPair>(rows, nz, nv, kc, k16, od, lane, xm, xo, pair);
       }
       xpar ^= 1;
-      if (sub == 0 && lane == 0) prm.out.k_scale[bh * nblk + s0c / kQKBlock] = skv;
+      store_block_scale<kPair>(prm.out.k_scale, kh, nblk, s0c / kQKBlock, skv, lane, sub);
       tc::mbar_arrive(cx.empty(st));
       if (!pass(cnt + 1)) break;
     }
@@ -1193,6 +1279,7 @@ constexpr int kShortMaxGroups = 8;                 // the portable cluster size
 constexpr int kShortThreads = kTeams * kTeamThreads;
 constexpr uint32_t kShortSmemBytes = 3 * kTileBytes + 128;  // Q, K, V tiles + alignment slack
 
+template <bool kPair>
 __global__ void __launch_bounds__(kShortThreads, 2)
     prologue_short_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const Params prm, int3 s_axis) {
@@ -1202,7 +1289,7 @@ __global__ void __launch_bounds__(kShortThreads, 2)
   __shared__ uint32_t vm[kWarps][kHeadDim / 2];  // per-warp max |v| bits, channel pairs
   __shared__ float xk_hi[kChunks][kHeadDim], xk_lo[kChunks][kHeadDim];  // second-half key sums
   __shared__ uint32_t xk_bits[kChunks][32];      // second-half magnitude bounds per lane
-  __shared__ float xa[kTeams * kWarps / 2][2];   // block amax exchange of each warp pair
+  __shared__ float xa[kTeams * kWarps / 2][2][2];  // block amax exchange of each warp pair (per head of a pair)
   __shared__ double g_sum[kHeadDim];    // this group's key sums (read by the whole cluster)
   __shared__ uint32_t g_max[kHeadDim];  // this group's max |v| bits
   __shared__ __align__(16) float h_mean[kHeadDim];
@@ -1239,7 +1326,8 @@ __global__ void __launch_bounds__(kShortThreads, 2)
     const uint64_t pol = tc::policy_evict_first();  // every tile is read once
     const CUtensorMap* maps[3] = {&tm_q, &tm_k, &tm_v};
     const int axes[3] = {s_axis.x, s_axis.y, s_axis.z};
-    const int32_t sc = static_cast<int32_t>(s_group), hc = static_cast<int32_t>(h), bc = static_cast<int32_t>(b);
+    const int32_t sc = static_cast<int32_t>(s_group), hc = static_cast<int32_t>((kPair ? 2 : 1) * h),
+                  bc = static_cast<int32_t>(b);
 #pragma unroll
     for (int n = 0; n < 3; ++n) {
       tc::mbar_arrive_expect_tx(cx.full(n), kTileBytes);
@@ -1282,20 +1370,24 @@ __global__ void __launch_bounds__(kShortThreads, 2)
     tc::cluster_arrive_relaxed();
     ok = wait_bar(cx, cx.full(0), 0) && ok;
     const float2 nz[4] = {};
-    int8_t* qc = prm.write_int8 ? prm.out.q_codes + bh * S_pad * kHeadDim : nullptr;
-    uint16_t* q16 = prm.out.q16 + bh * S_pad * kHeadDim;
-    const float s = nv == kHalfRows ? quantize_half_block<false, true>(q_rows, nz, kHalfRows, qc, q16, s0, lane,
-                                                                       &xa[pair][sub], &xa[pair][sub ^ 1], pair)
-                                    : quantize_half_block<false, false>(q_rows, nz, nv, qc, q16, s0, lane,
-                                                                        &xa[pair][sub], &xa[pair][sub ^ 1], pair);
-    if (sub == 0 && lane == 0) prm.out.q_scale[bh * nblk + s0c / kQKBlock] = s;
+    int8_t* qc;
+    uint16_t* q16;
+    const int64_t qh =
+        lane_codes<kPair>(prm, prm.write_int8 ? prm.out.q_codes : nullptr, prm.out.q16, bh, s0, lane, qc, q16);
+    constexpr int od = kOutDim<kPair>;
+    const float s = nv == kHalfRows
+                        ? quantize_half_block<false, true, kPair>(q_rows, nz, kHalfRows, qc, q16, od, lane,
+                                                                  &xa[pair][sub][0], &xa[pair][sub ^ 1][0], pair)
+                        : quantize_half_block<false, false, kPair>(q_rows, nz, nv, qc, q16, od, lane,
+                                                                   &xa[pair][sub][0], &xa[pair][sub ^ 1][0], pair);
+    store_block_scale<kPair>(prm.out.q_scale, qh, nblk, s0c / kQKBlock, s, lane, sub);
     tc::cluster_wait_acquire();
     tc::cluster_arrive_relaxed();  // team 0 reads no other CTA's shared memory
     asm volatile("bar.sync 2, %0;" ::"n"(kShortThreads) : "memory");  // the V scales are in h_vscale
     // V codes, transposed (4-channel lanes)
     v_codes_rows(v_rows, nv, lane, *reinterpret_cast<const float4*>(h_vscale + 4 * lane),
-                 *reinterpret_cast<const float4*>(h_vrcp + 4 * lane), prm.out.vt_codes + bh * kHeadDim * S_pad,
-                 S_pad, s0, [] {});
+                 *reinterpret_cast<const float4*>(h_vrcp + 4 * lane), lane_vt<kPair>(prm, bh, s0, lane), S_pad,
+                 [] {});
   } else {
     // the group's exact key sums
     ok = wait_bar(cx, cx.full(1), 0);
@@ -1352,33 +1444,39 @@ __global__ void __launch_bounds__(kShortThreads, 2)
       h_vscale[c] = vs;
       h_vrcp[c] = vs >= FLT_MIN ? __frcp_rn(vs) : 0.0f;
       if (g == 0) {
-        prm.out.k_mean[bh * kHeadDim + c] = mu;
-        prm.out.v_scale[bh * kHeadDim + c] = vs;
+        const int64_t head = out_head<kPair>(prm, bh, c / kOutDim<kPair>);
+        if (head >= 0) {
+          prm.out.k_mean[head * kOutDim<kPair> + (c & (kOutDim<kPair> - 1))] = mu;
+          prm.out.v_scale[head * kOutDim<kPair> + (c & (kOutDim<kPair> - 1))] = vs;
+        }
       }
     }
     asm volatile("bar.arrive 2, %0;" ::"n"(kShortThreads) : "memory");  // h_vscale to team 0
     asm volatile("bar.sync 11, %0;" ::"n"(kTeamThreads) : "memory");    // h_mean within team 1
     // K codes of k - mean
-    int8_t* kc = prm.write_int8 ? prm.out.k_codes + bh * S_pad * kHeadDim : nullptr;
-    uint16_t* k16 = prm.out.k16 + bh * S_pad * kHeadDim;
+    int8_t* kc;
+    uint16_t* k16;
+    const int64_t kh =
+        lane_codes<kPair>(prm, prm.write_int8 ? prm.out.k_codes : nullptr, prm.out.k16, bh, s0, lane, kc, k16);
+    constexpr int od = kOutDim<kPair>;
+    volatile float* xm = &xa[pair][sub][0];
+    volatile float* xo = &xa[pair][sub ^ 1][0];
     float skv;
     if (prm.smooth_k) {
       const float4* mp = reinterpret_cast<const float4*>(h_mean + 8 * (lane & 15));
       const float4 ma = mp[0], mb = mp[1];
       const float2 nmu[4] = {make_float2(-ma.x, -ma.y), make_float2(-ma.z, -ma.w), make_float2(-mb.x, -mb.y),
                              make_float2(-mb.z, -mb.w)};
-      skv = nv == kHalfRows ? quantize_half_block<true, true>(k_rows, nmu, kHalfRows, kc, k16, s0, lane,
-                                                              &xa[pair][sub], &xa[pair][sub ^ 1], pair)
-                            : quantize_half_block<true, false>(k_rows, nmu, nv, kc, k16, s0, lane, &xa[pair][sub],
-                                                               &xa[pair][sub ^ 1], pair);
+      skv = nv == kHalfRows
+                ? quantize_half_block<true, true, kPair>(k_rows, nmu, kHalfRows, kc, k16, od, lane, xm, xo, pair)
+                : quantize_half_block<true, false, kPair>(k_rows, nmu, nv, kc, k16, od, lane, xm, xo, pair);
     } else {
       const float2 nz[4] = {};
-      skv = nv == kHalfRows ? quantize_half_block<false, true>(k_rows, nz, kHalfRows, kc, k16, s0, lane,
-                                                               &xa[pair][sub], &xa[pair][sub ^ 1], pair)
-                            : quantize_half_block<false, false>(k_rows, nz, nv, kc, k16, s0, lane, &xa[pair][sub],
-                                                                &xa[pair][sub ^ 1], pair);
+      skv = nv == kHalfRows
+                ? quantize_half_block<false, true, kPair>(k_rows, nz, kHalfRows, kc, k16, od, lane, xm, xo, pair)
+                : quantize_half_block<false, false, kPair>(k_rows, nz, nv, kc, k16, od, lane, xm, xo, pair);
     }
-    if (sub == 0 && lane == 0) prm.out.k_scale[bh * nblk + s0c / kQKBlock] = skv;
+    store_block_scale<kPair>(prm.out.k_scale, kh, nblk, s0c / kQKBlock, skv, lane, sub);
   }
   if (!ok) {
     // let every copy land before the CTA exits
@@ -1392,10 +1490,12 @@ __global__ void __launch_bounds__(kShortThreads, 2)
 }
 
 struct ScratchLayout {
-  size_t done_off, ready_off, ksum_off, vmax_off, vrcp_off, header, total;
+  size_t done_off, ready_off, ksum_off, vmax_off, vrcp_off, hstat_off, header, total;
 };
 
-ScratchLayout scratch_layout(int64_t B, int64_t S, int64_t H) {
+// H: the (virtual) heads per batch; pair: head-pair mode, which adds each
+// virtual head's key mean and V scales for the codes items.
+ScratchLayout scratch_layout(int64_t B, int64_t S, int64_t H, bool pair) {
   const int64_t G = div_up(S, kItemTokens);
   const size_t NH = static_cast<size_t>(B * H);
   const size_t n = NH * static_cast<size_t>(G) * kHeadDim;
@@ -1407,7 +1507,8 @@ ScratchLayout scratch_layout(int64_t B, int64_t S, int64_t H) {
   l.ksum_off = l.header;
   l.vmax_off = l.ksum_off + r256(n * sizeof(double));
   l.vrcp_off = l.vmax_off + r256(n * sizeof(float));
-  l.total = l.vrcp_off + r256(NH * kHeadDim * sizeof(float));
+  l.hstat_off = l.vrcp_off + r256(NH * kHeadDim * sizeof(float));
+  l.total = l.hstat_off + (pair ? r256(NH * 2 * kHeadDim * sizeof(float)) : 0);
   return l;
 }
 
@@ -1427,27 +1528,83 @@ int make_input_map(CUtensorMap* m, const Bf16In& t, int64_t B, int64_t S, int64_
   return s_first ? 1 : 2;
 }
 
+// 4-D bf16 map over one head-dimension-64 input for head-pair mode: dims
+// (channel, h, s, b) with the input's own strides, in whatever order they
+// come, and boxes of 64 channels x 2 heads x 128 tokens, which land in shared
+// memory as 128 rows of (head 2hp, head 2hp + 1): the 128-channel tile of
+// virtual head hp. A missing second head (odd H) reads as zeros.
+bool make_pair_map(CUtensorMap* m, const Bf16In& t, int64_t B, int64_t S, int64_t H) {
+  const uint64_t dims[4] = {static_cast<uint64_t>(kHeadDim / 2), static_cast<uint64_t>(H), static_cast<uint64_t>(S),
+                            static_cast<uint64_t>(B)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(t.sh * 2), static_cast<uint64_t>(t.ss * 2),
+                               static_cast<uint64_t>(t.sb * 2)};
+  const uint32_t box[4] = {kHeadDim / 2, 2u, static_cast<uint32_t>(kItemTokens), 1u};
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 }  // namespace
 
 bool prologue_uses_scratch(int64_t S, int64_t D) {
-  return D != kHeadDim || div_up(S, kItemTokens) > kShortMaxGroups;
+  (void)D;  // both head dimensions use the cluster kernel for short sequences
+  return div_up(S, kItemTokens) > kShortMaxGroups;
 }
 
 size_t prologue_scratch_bytes(int64_t B, int64_t S, int64_t H, int64_t D) {
-  return D == kHeadDim ? scratch_layout(B, S, H).total : prologue64_scratch_bytes(B, S, H);
+  return D == kHeadDim ? scratch_layout(B, S, H, false).total : scratch_layout(B, S, div_up(H, 2), true).total;
 }
+
+namespace {
+
+template <bool kPair>
+cudaError_t launch_prologue_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const Params& p,
+                              int3 axes, void* scratch, size_t header, cudaStream_t stream) {
+  cudaError_t e;
+  if (p.G <= kShortMaxGroups) {
+    // short sequences: one cluster per head, no scratch
+    if ((e = set_smem_limit_once(reinterpret_cast<const void*>(prologue_short_kernel<kPair>),
+                                 static_cast<int>(kShortSmemBytes))) != cudaSuccess)
+      return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.G * p.NH));
+    cfg.blockDim = dim3(kShortThreads);
+    cfg.dynamicSmemBytes = kShortSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.G);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prologue_short_kernel<kPair>, tq, tk, tv, p, axes);
+  }
+  if ((e = cudaMemsetAsync(scratch, 0, header, stream)) != cudaSuccess) return e;
+  if ((e = set_smem_limit_once(reinterpret_cast<const void*>(prologue_kernel<kPair>), static_cast<int>(kSmemBytes))) !=
+      cudaSuccess)
+    return e;
+  const int sms = sm_count_current();
+  const int grid = static_cast<int>(p.total < sms ? p.total : sms);
+  prologue_kernel<kPair><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p, axes);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, int64_t B, int64_t S, int64_t H,
                             int64_t D, bool smooth_k, const Bundle& out, void* scratch, bool write_int8,
                             int* dev_err, cudaStream_t stream) {
-  if (D != kHeadDim) return launch_prologue64(q, k, v, B, S, H, smooth_k, out, scratch, write_int8, stream);
-  const ScratchLayout l = scratch_layout(B, S, H);
+  if (D != kHeadDim && D != kHeadDim / 2) return cudaErrorInvalidValue;
+  // head dimension 64 runs as head pairs: ceil(H / 2) virtual heads of 128 channels
+  const bool pair = D != kHeadDim;
+  const int64_t Hv = pair ? div_up(H, 2) : H;
+  const ScratchLayout l = scratch_layout(B, S, Hv, pair);
   char* sc = static_cast<char*>(scratch);
   Params p;
   p.S = S;
   p.S_pad = padded_len(S);
-  p.H = H;
-  p.NH = B * H;
+  p.H = Hv;
+  p.Hr = H;
+  p.NH = B * Hv;
   p.G = div_up(S, kItemTokens);
   p.total = 2 * p.NH * p.G;
   // every stats item comes before every codes item (lag = all heads).
@@ -1466,40 +1623,18 @@ cudaError_t launch_prologue(const Bf16In& q, const Bf16In& k, const Bf16In& v, i
   p.ksum = reinterpret_cast<double*>(sc + l.ksum_off);
   p.vmax = reinterpret_cast<float*>(sc + l.vmax_off);
   p.vrcp = reinterpret_cast<float*>(sc + l.vrcp_off);
+  p.hstat_v = pair ? reinterpret_cast<float*>(sc + l.hstat_off) : nullptr;
   p.dev_err = dev_err;
   CUtensorMap tq, tk, tv;
+  if (pair) {
+    if (!make_pair_map(&tq, q, B, S, H) || !make_pair_map(&tk, k, B, S, H) || !make_pair_map(&tv, v, B, S, H))
+      return cudaErrorInvalidValue;
+    return launch_prologue_t<true>(tq, tk, tv, p, make_int3(2, 2, 2), scratch, l.header, stream);
+  }
   const int aq = make_input_map(&tq, q, B, S, H), ak = make_input_map(&tk, k, B, S, H),
             av = make_input_map(&tv, v, B, S, H);
   if (aq == 0 || ak == 0 || av == 0) return cudaErrorInvalidValue;
-  const int3 axes = make_int3(aq, ak, av);
-  cudaError_t e;
-  if (p.G <= kShortMaxGroups) {
-    // short sequences: one cluster per head, no scratch
-    if ((e = set_smem_limit_once(reinterpret_cast<const void*>(prologue_short_kernel),
-                                 static_cast<int>(kShortSmemBytes))) != cudaSuccess)
-      return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.G * p.NH));
-    cfg.blockDim = dim3(kShortThreads);
-    cfg.dynamicSmemBytes = kShortSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.G);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prologue_short_kernel, tq, tk, tv, p, axes);
-  }
-  if ((e = cudaMemsetAsync(scratch, 0, l.header, stream)) != cudaSuccess) return e;
-  if ((e = set_smem_limit_once(reinterpret_cast<const void*>(prologue_kernel), static_cast<int>(kSmemBytes))) !=
-      cudaSuccess)
-    return e;
-  const int sms = sm_count_current();
-  const int grid = static_cast<int>(p.total < sms ? p.total : sms);
-  prologue_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p, axes);
-  return cudaGetLastError();
+  return launch_prologue_t<false>(tq, tk, tv, p, make_int3(aq, ak, av), scratch, l.header, stream);
 }
 
 }  // namespace sage

@@ -57,6 +57,13 @@ def test_size_queries(lib):
     # then fp64 + fp32 per (head, 128-token group, channel), then the fp32
     # reciprocals of each head's 128 V scales
     assert sc == 256 + 2 * 256 + 28 * 128 * 128 * 8 + 28 * 128 * 128 * 4 + 28 * 128 * 4
+    # head dimension 64 runs as 14 head pairs of 128 channels, plus each
+    # pair's key mean and V scales for the codes items
+    rc, sc64 = _sizes(lib, "sage_quantize_scratch_size", B, S, H, 64)
+    assert rc == OK
+    assert sc64 == 256 + 2 * 256 + 14 * 128 * 128 * 8 + 14 * 128 * 128 * 4 + 14 * 128 * 4 + 14 * 256 * 4
+    assert _sizes(lib, "sage_quantize_scratch_size", 1, 1000, 3, 64)[1] == (
+        256 + 2 * 256 + 2 * 8 * 128 * 8 + 2 * 8 * 128 * 4 + 2 * 128 * 4 + 2 * 256 * 4)
     assert _sizes(lib, "sage_workspace_size", 1, 100, 2, 96)[0] == HEAD_DIM
     assert _sizes(lib, "sage_workspace_size", 1, 100, 2, 64)[0] == OK
     assert _sizes(lib, "sage_workspace_size", -1, 100, 2, 128)[0] == SHAPE

@@ -31,9 +31,11 @@ def _prologue(q, k, v, layout, smooth, heads=None):
     return qz
 
 
-@pytest.mark.parametrize("s_len", [1, 31, 33, 129, 255, 1000])
+@pytest.mark.parametrize("s_len", [1, 31, 33, 129, 255, 1000, 1025, 1300])
 @pytest.mark.parametrize("smooth", [True, False])
 def test_prologue_d64_ragged(sage_lib, s_len, smooth):
+    # 3 heads: the prologue runs head pairs, the second pair missing its
+    # second head; up to 1024 tokens the cluster kernel, beyond the persistent one
     w = custom(2, 3, s_len, seed_index=1100 + s_len, k_offset_std=2.0, D=64)
     q, k, v = make_qkv(w, "cuda")
     _prologue(q, k, v, "NHD", smooth)
@@ -44,11 +46,28 @@ def test_prologue_d64_image_size_and_hnd(sage_lib):
     _prologue(q, k, v, "NHD", True)
     q, k, v = make_qkv(custom(2, 4, 700, seed_index=1150, k_offset_std=3.0, D=64), "cuda", "HND")
     _prologue(q, k, v, "HND", True)
+    q, k, v = make_qkv(custom(2, 5, 1500, seed_index=1151, k_offset_std=3.0, D=64), "cuda", "HND")
+    _prologue(q, k, v, "HND", True)
 
 
-def test_prologue_d64_edge_values(sage_lib):
-    rng = np.random.default_rng(64)
-    S, H = 300, 2
+@pytest.mark.parametrize("s_len", [300, 1300])
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_prologue_d64_head_view_past_the_last_pair(sage_lib, s_len, layout):
+    """Heads 0..2 of a 5-head tensor (a view: the head stride and the batch
+    stride are the full tensor's). The last pair's second head lies outside
+    the view; its memory holds head 3 of the full tensor (large values here),
+    which must not leak into any output."""
+    w = custom(2, 5, s_len, seed_index=1160 + s_len, k_offset_std=2.0, D=64)
+    q, k, v = make_qkv(w, "cuda", layout)
+    ax = 2 if layout == "NHD" else 1
+    for t in (q, k, v):
+        t.narrow(ax, 3, 1).mul_(64.0)  # head 3: never read
+    view = [t.narrow(ax, 0, 3) for t in (q, k, v)]
+    _prologue(*view, layout, True)
+
+@pytest.mark.parametrize("S,H", [(300, 2), (1300, 3)])
+def test_prologue_d64_edge_values(sage_lib, S, H):
+    rng = np.random.default_rng(64 + S)
     q = rng.standard_normal((1, S, H, 64)).astype(np.float32)
     k = rng.standard_normal((1, S, H, 64)).astype(np.float32) + 3.0
     v = rng.standard_normal((1, S, H, 64)).astype(np.float32)
@@ -68,12 +87,13 @@ def test_prologue_d64_edge_values(sage_lib):
         _prologue(qt, kt, vt, "NHD", smooth)
 
 
-def test_prologue_d64_key_sum_exponent_spread(sage_lib):
+@pytest.mark.parametrize("S", [1000, 2100])
+def test_prologue_d64_key_sum_exponent_spread(sage_lib, S):
     # Chunks whose key magnitudes in a channel span 20 to 50 binades: the
     # float-pair chunk sums are taken where they are exact and the fp64 left-to-
     # right sums elsewhere, per channel; ties of x/s and subnormal values mixed in.
-    rng = np.random.default_rng(640)
-    S, H = 1000, 2
+    rng = np.random.default_rng(640 + S)
+    H = 2
     q = rng.standard_normal((1, S, H, 64)).astype(np.float32)
     k = rng.standard_normal((1, S, H, 64)).astype(np.float32)
     v = rng.standard_normal((1, S, H, 64)).astype(np.float32)
