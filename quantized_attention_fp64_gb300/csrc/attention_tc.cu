@@ -110,6 +110,13 @@ static_assert(SmemTail<128>::kBytes <= 232448u, "shared memory of one CTA: at mo
 __host__ __device__ constexpr uint32_t col_s(int i) { return 128u * static_cast<uint32_t>(i); }
 template <int D>
 __host__ __device__ constexpr uint32_t col_o(int i) { return 256u + static_cast<uint32_t>(D) * static_cast<uint32_t>(i); }
+// At D = 64 the 128 columns past O hold P of each query tile, two buffers of
+// 32 columns (128 e4m3 keys of a row, four per column) at 384 + 64*i + 32*b:
+// PV reads P from tensor memory, and the softmax writes P of step j while PV
+// of step j-1 still reads the other buffer.
+__host__ __device__ constexpr uint32_t col_p(int i, int b) {
+  return 384u + 64u * static_cast<uint32_t>(i) + 32u * static_cast<uint32_t>(b);
+}
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
@@ -279,14 +286,19 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t 
 }
 
 // O_i (+)= P_i V for one 128-key tile: 4 MMAs of M = 128, N = D, K = 32;
-// P_i (e4m3, written by the softmax warps) and V^T both in shared memory,
-// 128-byte swizzled.
+// V^T in shared memory, 128-byte swizzled; P_i (e4m3, written by the softmax
+// warps) in shared memory in the same layout at D = 128 (dp), in tensor
+// memory at D = 64 (tp: its first column; 32 keys are 8 columns).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint64_t dp, uint64_t dv, bool acc) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint64_t dp, uint32_t tp, uint64_t dv, bool acc) {
   constexpr uint32_t idesc = D == 128 ? tc::kIdescM128N128 : tc::kIdescM128N64;
 #pragma unroll
-  for (int ks = 0; ks < 4; ++ks)
-    tc::mma_f8_ss(d_tmem, desc_at(dp, 32u * ks), desc_at(dv, 32u * ks), idesc, (acc || ks > 0) ? 1u : 0u);
+  for (int ks = 0; ks < 4; ++ks) {
+    if constexpr (D == 64)
+      tc::mma_f8_ts(d_tmem, tp + 8u * ks, desc_at(dv, 32u * ks), idesc, (acc || ks > 0) ? 1u : 0u);
+    else
+      tc::mma_f8_ss(d_tmem, desc_at(dp, 32u * ks), desc_at(dv, 32u * ks), idesc, (acc || ks > 0) ? 1u : 0u);
+  }
 }
 
 // One lane of the warp, chosen by the hardware (elect.sync).
@@ -303,11 +315,13 @@ __device__ __forceinline__ bool elect_one() {
 // running maximum m and row sum l, waits until the previous PV has finished
 // with P and O, writes e4m3(p448) into the shared-memory P tile and rescales O
 // when the maximum grew. kTail masks keys at or past nvalid (the last tile of a
-// ragged S). Returns false if a bounded wait ran out.
+// ragged S). At D = 64, P goes to this step's tensor-memory buffer tP instead
+// (the previous PV reads the other one), before the wait for that PV, which
+// only the O rescale needs. Returns false if a bounded wait ran out.
 template <int D, bool kTail, bool kCorr>
-__device__ __forceinline__ bool softmax_tile(const Ctx& cx, int i, uint32_t tS, uint32_t tO, float* alpha_row,
-                                             uint8_t* p_row, int row, const float (&cb)[4], int nvalid, bool first,
-                                             uint32_t& pv_cnt, float& m, float& l) {
+__device__ __forceinline__ bool softmax_tile(const Ctx& cx, int i, uint32_t tS, uint32_t tO, uint32_t tP,
+                                             float* alpha_row, uint8_t* p_row, int row, const float (&cb)[4],
+                                             int nvalid, bool first, uint32_t& pv_cnt, float& m, float& l) {
   uint32_t sr[4][32];
 #pragma unroll
   for (int b = 0; b < 4; ++b) tc::tmem_ld32(tS + 32u * b, sr[b]);
@@ -364,6 +378,37 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& cx, int i, uint32_t tS, 
   }
   l = l * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
   m = m_new;
+  if constexpr (D == 64) {
+    // P of this step into its buffer: the PV that last read it (two steps
+    // back) completed before the previous step's wait below returned, and the
+    // unit's last PV before the unit's epilogue
+    tc::tmem_st32(tP, pw);
+    if (!first) {
+      // the previous PV must be done with O before the rescale
+      if (!wait_bar_warp(cx, cx.bar(kBarPVDone + i), pv_cnt & 1u)) return false;
+      ++pv_cnt;
+      tc::tc_fence_after();
+      if (__any_sync(0xffffffffu, grew)) {
+        uint32_t o[D / 32][32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tc::tmem_ld32(tO + 32u * c, o[c]);
+        tc::tmem_wait_ld();
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const float2 r = __fmul2_rn(make_float2(__uint_as_float(o[c][k]), __uint_as_float(o[c][k + 1])), a2);
+            o[c][k] = __float_as_uint(r.x);
+            o[c][k + 1] = __float_as_uint(r.y);
+          }
+          tc::tmem_st32(tO + 32u * c, o[c]);
+        }
+      }
+    }
+    tc::tmem_wait_st();  // P (and O) written before the caller signals the MMA issuer
+    return true;
+  }
   // the previous PV of this tile must be done with P (shared memory) and O
   if (!first) {
     if (!wait_bar_warp(cx, cx.bar(kBarPVDone + i), pv_cnt & 1u)) return false;
@@ -592,7 +637,7 @@ __global__ void __launch_bounds__(threads_of<kCorr>(), 1)
               }
               tc::tc_fence_after();
               if (leader) {
-                issue_pv<D>(d_o, dp, desc_at(dv0, vs * L::kTileV), jj > 0);
+                issue_pv<D>(d_o, dp, tmem + col_p(i, static_cast<int>(jj & 1)), desc_at(dv0, vs * L::kTileV), jj > 0);
                 tc::mma_commit(cx.bar(kBarPVDone + i));
                 tc::mma_commit(cx.bar(kBarVEmpty + vs));
               }
@@ -679,6 +724,7 @@ __global__ void __launch_bounds__(threads_of<kCorr>(), 1)
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_addr + col_s(i);
     const uint32_t tO = tmem + lane_addr + col_o<D>(i);
+    const uint32_t tP0 = tmem + lane_addr + col_p(i, 0);  // D = 64: this row's P buffers
     uint8_t* p_row = smem + L::kOffP + static_cast<uint32_t>(i) * kTile8 + row * 128;
     float* alpha_row = reinterpret_cast<float*>(smem + T::kOffAlpha) + i * 128 + row;
     const int64_t nblk = prm.S_pad / kQKBlock;
@@ -726,10 +772,10 @@ __global__ void __launch_bounds__(threads_of<kCorr>(), 1)
         int64_t lim = below_s < kKeyTile ? below_s : kKeyTile;
         if (diagonal && lim > row + 1) lim = row + 1;
         ok = !(diagonal || below_s < kKeyTile)
-                 ? softmax_tile<D, false, kCorr>(cx, i, tS, tO, alpha_row, p_row, row, cb, kKeyTile, j == 0, pv_cnt,
-                                                 m, l)
-                 : softmax_tile<D, true, kCorr>(cx, i, tS, tO, alpha_row, p_row, row, cb, static_cast<int>(lim),
-                                                j == 0, pv_cnt, m, l);
+                 ? softmax_tile<D, false, kCorr>(cx, i, tS, tO, tP0 + 32u * static_cast<uint32_t>(j & 1), alpha_row,
+                                                 p_row, row, cb, kKeyTile, j == 0, pv_cnt, m, l)
+                 : softmax_tile<D, true, kCorr>(cx, i, tS, tO, tP0 + 32u * static_cast<uint32_t>(j & 1), alpha_row,
+                                                p_row, row, cb, static_cast<int>(lim), j == 0, pv_cnt, m, l);
         if (!ok) break;
         tc::tc_fence_before();
         tc::mbar_arrive(cx.bar(kBarPFull + i));
