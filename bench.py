@@ -348,7 +348,7 @@ def run_profile(args):
     q, k, v = make_qkv(w, "cuda")
     for _ in range(args.warmup + 1):
         qz = quantize(q, k, v, "NHD", w.smooth_k)
-        attention(qz, 1.0 / math.sqrt(128.0), is_causal=args.causal)
+        attention(qz, 1.0 / math.sqrt(float(w.D)), is_causal=args.causal)
     torch.cuda.synchronize()
     print(f"profiled {args.workload}" + (" (causal)" if args.causal else ""))
     return 0
