@@ -31,11 +31,11 @@ SAGE_ERR_TOO_LARGE = -14
 
 
 def _noalloc(lib, q, k, v, smooth_k):
-    B, S, H = q.shape[0], q.shape[1], q.shape[2]
-    qz = alloc_bundle(B, S, H, q.device)
+    B, S, H, D = q.shape
+    qz = alloc_bundle(B, S, H, q.device, D)
     bundle = qz.c_struct()
     rc = lib.sage_quantize_noalloc(ctypes.byref(_bf16_tensor(q, "NHD")), ctypes.byref(_bf16_tensor(k, "NHD")),
-                                   ctypes.byref(_bf16_tensor(v, "NHD")), B, S, H, 128, int(smooth_k),
+                                   ctypes.byref(_bf16_tensor(v, "NHD")), B, S, H, D, int(smooth_k),
                                    ctypes.byref(bundle), _stream(q.device))
     assert rc == 0, lib.sage_strerror(rc)
     return qz
@@ -61,7 +61,11 @@ def test_noalloc_persistent_path_back_to_back(sage_lib):
     problems = [(custom(1, 4, 2200, seed_index=903, k_offset_std=2.0), True),
                 (custom(1, 3, 300, seed_index=904, k_offset_std=2.0), True),
                 (custom(2, 3, 1500, seed_index=905, k_offset_std=0.0), False),
-                (custom(1, 4, 2200, seed_index=906, k_offset_std=2.0), True)]
+                (custom(1, 4, 2200, seed_index=906, k_offset_std=2.0), True),
+                # head dimension 64: head pairs, with an odd head count (the
+                # scratch also holds each pair's key mean and V scales)
+                (custom(2, 5, 1700, seed_index=907, k_offset_std=2.0, D=64), True),
+                (custom(1, 4, 2200, seed_index=908, k_offset_std=1.0), True)]
     for w, smooth in problems:
         q, k, v = make_qkv(w, "cuda")
         got = _noalloc(lib, q, k, v, smooth)
