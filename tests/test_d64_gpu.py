@@ -50,6 +50,14 @@ def test_prologue_d64_image_size_and_hnd(sage_lib):
     _prologue(q, k, v, "HND", True)
 
 
+@pytest.mark.parametrize("s_len", [100, 1500])
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_prologue_d64_single_head(sage_lib, s_len, layout):
+    # one head: the only pair's second head lies past the tensor's head extent
+    q, k, v = make_qkv(custom(2, 1, s_len, seed_index=1170 + s_len, k_offset_std=2.0, D=64), "cuda", layout)
+    _prologue(q, k, v, layout, True)
+
+
 @pytest.mark.parametrize("s_len", [300, 1300])
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
 def test_prologue_d64_head_view_past_the_last_pair(sage_lib, s_len, layout):
