@@ -50,6 +50,13 @@
  *    and padded scale blocks are written as zero.
  *  - S = 0 (or B = 0 or H = 0) is an empty problem: validated, nothing
  *    launched, SAGE_OK.
+ *  - Device entries work on the current device (cudaGetDevice) in its
+ *    runtime primary context: a thread's first such call on a device makes
+ *    that context current in the thread (cudaSetDevice), which the
+ *    tensor-map encoding before the first launch needs. A driver-API
+ *    context the thread had made current is replaced by it. Calls from
+ *    several threads are safe; work enqueued on one stream runs in the
+ *    order the calls enqueued it.
  */
 #ifndef SAGE_H
 #define SAGE_H
