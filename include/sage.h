@@ -55,8 +55,8 @@
  *    that context current in the thread (cudaSetDevice), which the
  *    tensor-map encoding before the first launch needs. A driver-API
  *    context the thread had made current is replaced by it. Calls from
- *    several threads are safe; work enqueued on one stream runs in the
- *    order the calls enqueued it.
+ *    several threads are safe as long as they do not share a scratch or
+ *    workspace buffer (see sage_sageattn).
  */
 #ifndef SAGE_H
 #define SAGE_H
@@ -279,6 +279,11 @@ SAGE_API int sage_attention_simt(const sage_quantized* in, int64_t B, int64_t S,
  * into out. Shapes and strides are given in the order of
  * tensor_layout: "NHD" = [B, S, H, D], "HND" = [B, H, S, D]; strides are in
  * elements. out has q's shape with out_strides.
+ * workspace_dev: at least sage_workspace_size bytes, 256-byte aligned. The
+ * call enqueues two kernels that pass the quantized bundle through it, so
+ * calls that share a workspace must not be enqueued concurrently from
+ * different threads (their kernels could interleave on the stream); reusing
+ * it from one thread in stream order is safe.
  * sm_scale: NaN selects 1/sqrt(D); otherwise it must be finite and > 0.
  * Rejected with an error and nothing launched: is_causal != 0 (CAUSAL),
  * return_lse != 0 (LSE), any dtype other than BF16 (DTYPE), D != 128
