@@ -165,6 +165,24 @@ def test_sageattn_ex_d64_and_page_entry_rejects(sage_lib):
         sageattn(q, k, v)   # the pages' entry: head dimension 128 only
 
 
+@pytest.mark.parametrize("s_len", [700, 2100])
+def test_sageattn_ex_d64_hnd_repeated(sage_lib, s_len):
+    """HND at D = 64 through sageattn_ex, unmasked, called twice with one
+    signature (the second call runs from the binding's kept arguments): both
+    calls equal, and the output within the tolerances of the oracle's
+    emulation on sampled heads, for both prologue kernels."""
+    w = custom(2, 5, s_len, seed_index=1270 + s_len, k_offset_std=2.0, D=64)
+    q, k, v = make_qkv(w, "cuda", "HND")
+    first = sageattn_ex(q, k, v, tensor_layout="HND", sm_scale=SM64)
+    again = sageattn_ex(q, k, v, tensor_layout="HND", sm_scale=SM64)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    assert torch.equal(first, again)
+    qn, kn, vn = to_np(q), to_np(k), to_np(v)
+    ref = quantize_tensors(qn, kn, vn, "HND", True)
+    check_attention(to_np(first), qn, kn, vn, "HND", ref, SM64, [(0, 0), (1, 4)])
+
+
 def test_noalloc_d64_matches_quantize(sage_lib):
     lib = _lib.load()
     w = custom(1, 5, 777, seed_index=1260, k_offset_std=1.0, D=64)
